@@ -1,0 +1,269 @@
+"""Float64 CPU oracle for causal grouped-query attention with sigmoid output gating.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's CPU
+baseline may import this module.  It shares no code with the CUDA library: it
+receives float64 numpy arrays (exact copies of the bf16 inputs) and computes
+the plain definition, row by row, without blocking over keys, fusion or an
+online softmax.
+
+What it computes (for every batch b, query head h, query row i):
+
+    g      = h // (Hq // Hkv)                      KV head of query head h
+    V_i    = { j : j < lim_i }                     keys row i may see
+    s_j    = (Q[b,h,i,:] . K[b,g,j,:]) / 16        j in V_i      (1/16 = 1/sqrt(256))
+    m      = max_j s_j,  p_j = exp(s_j - m),  l = sum_j p_j
+    o      = sum_j p_j V[b,g,j,:] / l
+    out    = o * 1 / (1 + exp(-G[b,h,i,:]))        sigmoid output gate
+    lse    = m + ln l
+
+Sources (page, section):
+  * TensorFold PR #1009, "Receipt", attention contract paragraph: the kernels are
+    checked against float64 gated attention at the 24/4 and 16/2 head shapes;
+    masked future keys must not contaminate a row (the -Inf x 0 prediction in the
+    same PR's second comment).
+  * TensorFold PR #1009, "Design: one engine": gated full attention layers.
+  * DS4Server issue113 README, opening rule: query heads inside each KV group,
+    head chunks of min(GQA, 32/rows) with remainders, concatenated in head order.
+  * The formula, scale 1/16 and the causal/offset mask as the task states them.
+
+Readings where the pages are silent (each listed in the design notes):
+  * the gate is elementwise, G has the shape of the output;
+  * query head h uses KV head h // GQA (consecutive grouping);
+  * prefill row i sits at absolute position kv_offset + i and sees keys
+    j <= kv_offset + i;
+  * decode/verify: kv_lens[b] counts the verify rows, row i of r_b rows sees
+    keys j < kv_lens[b] - r_b + i + 1;
+  * a row that sees no key outputs zeros and lse = -inf (float64 would give 0/0);
+  * keys a row does not see are excluded from its sums: the row's key range is
+    sliced, and inside a block of rows a key another row of the block sees gets
+    probability exactly 0 for this row (its V row is finite by the input contract,
+    since some row of the call sees it), so the sum is the excluded sum.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+HEAD_DIM = 256
+SCALE = 1.0 / 16.0          # 1/sqrt(head_dim)
+ROW_BLOCK = 256             # rows evaluated together; rows are independent
+
+
+def sigmoid(x):
+    """Elementwise logistic function in float64."""
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def kv_head_of(h: int, Hq: int, Hkv: int) -> int:
+    """KV head serving query head h: consecutive groups of GQA = Hq/Hkv heads."""
+    return h // (Hq // Hkv)
+
+
+def prefill_visible(i: int, kv_offset: int) -> int:
+    """Number of keys prompt row i may see: keys 0..kv_offset+i."""
+    return kv_offset + i + 1
+
+
+def verify_visible(i: int, rows: int, kv_len: int) -> int:
+    """Number of keys verify row i (0-based of `rows`) may see: the cache holds
+    kv_len keys including the rows themselves, so the row sits at absolute
+    position kv_len - rows + i."""
+    return kv_len - rows + i + 1
+
+
+def attend_rows(q_rows, K, V, g_rows, lims):
+    """Gated attention of a block of query rows against one KV head.
+
+    q_rows [n,D], g_rows [n,D] or None, K,V [L,D], lims [n] (keys each row sees).
+    Returns (out [n,D], lse [n]) in float64.
+    """
+    q_rows = np.asarray(q_rows, dtype=np.float64)
+    lims = np.asarray(lims, dtype=np.int64)
+    n, D = q_rows.shape
+    out = np.zeros((n, D))
+    lse = np.full(n, -np.inf)
+    kmax = int(lims.max()) if n else 0
+    if kmax <= 0:
+        return out, lse
+    Kb = np.asarray(K[:kmax], dtype=np.float64)
+    Vb = np.asarray(V[:kmax], dtype=np.float64)
+    s = (q_rows @ Kb.T) * SCALE                      # [n, kmax]
+    seen = np.arange(kmax)[None, :] < lims[:, None]  # [n, kmax]
+    s = np.where(seen, s, -np.inf)
+    live = lims > 0
+    m = np.where(live, s.max(axis=1), 0.0)
+    p = np.where(seen, np.exp(s - m[:, None]), 0.0)
+    l = p.sum(axis=1)
+    o = np.zeros((n, D))
+    o[live] = (p[live] @ Vb) / l[live, None]
+    if g_rows is not None:
+        o = o * sigmoid(np.asarray(g_rows, dtype=np.float64))
+    out[live] = o[live]
+    lse[live] = m[live] + np.log(l[live])
+    return out, lse
+
+
+def prefill(Q, K, V, G, kv_offset=0, rows=None):
+    """Prompt-row attention.  Q,G [B,Hq,Lq,D]; K,V [B,Hkv,Lkv,D] (float64-able).
+
+    ``rows``: optional iterable of (b, h, i) to evaluate only those rows (for
+    sampled checks at full size).  Returns (out, lse): full arrays
+    [B,Hq,Lq,D]/[B,Hq,Lq] when rows is None, else arrays [n,D]/[n] in the order
+    given.
+    """
+    B, Hq, Lq, D = Q.shape
+    Hkv, Lkv = K.shape[1], K.shape[2]
+    assert D == HEAD_DIM and Hq % Hkv == 0 and kv_offset + Lq <= Lkv
+    if rows is not None:
+        rows = list(rows)
+        out = np.zeros((len(rows), D))
+        lse = np.zeros(len(rows))
+        for n, (b, h, i) in enumerate(rows):
+            g = kv_head_of(h, Hq, Hkv)
+            o, s = attend_rows(np.asarray(Q[b, h, i:i + 1], dtype=np.float64), K[b, g], V[b, g],
+                               None if G is None else G[b, h, i:i + 1],
+                               [prefill_visible(i, kv_offset)])
+            out[n], lse[n] = o[0], s[0]
+        return out, lse
+    out = np.zeros((B, Hq, Lq, D))
+    lse = np.zeros((B, Hq, Lq))
+    for b in range(B):
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            for r0 in range(0, Lq, ROW_BLOCK):
+                r1 = min(Lq, r0 + ROW_BLOCK)
+                lims = [prefill_visible(i, kv_offset) for i in range(r0, r1)]
+                o, s = attend_rows(Q[b, h, r0:r1], K[b, g], V[b, g],
+                                   None if G is None else G[b, h, r0:r1], lims)
+                out[b, h, r0:r1] = o
+                lse[b, h, r0:r1] = s
+    return out, lse
+
+
+def decode(Q, Kc, Vc, G, kv_lens, cu_rows=None, rows=None):
+    """Decode (one row per sequence) and chain verify (rows causal within the
+    sequence's new rows) against a contiguous cache.
+
+    Q,G [T,Hq,D] token-major; Kc,Vc [B,Hkv,Lcap,D]; kv_lens [B] (includes the
+    rows); cu_rows [B+1] or None (one row per sequence).  ``rows``: optional
+    iterable of (t, h) to evaluate only those outputs.  Returns (out, lse) of
+    shapes [T,Hq,D]/[T,Hq] or [n,D]/[n].
+    """
+    T, Hq, D = Q.shape
+    B, Hkv = Kc.shape[0], Kc.shape[1]
+    kv_lens = [int(x) for x in kv_lens]
+    cu = list(range(B + 1)) if cu_rows is None else [int(x) for x in cu_rows]
+    assert D == HEAD_DIM and Hq % Hkv == 0 and cu[-1] == T
+    seq_of = np.zeros(T, dtype=np.int64)
+    for b in range(B):
+        seq_of[cu[b]:cu[b + 1]] = b
+
+    def lim_of(t):
+        b = int(seq_of[t])
+        return verify_visible(t - cu[b], cu[b + 1] - cu[b], kv_lens[b])
+
+    if rows is not None:
+        rows = list(rows)
+        out = np.zeros((len(rows), D))
+        lse = np.zeros(len(rows))
+        for n, (t, h) in enumerate(rows):
+            b = int(seq_of[t])
+            g = kv_head_of(h, Hq, Hkv)
+            o, s = attend_rows(np.asarray(Q[t, h:h + 1], dtype=np.float64), Kc[b, g], Vc[b, g],
+                               None if G is None else G[t, h:h + 1], [lim_of(t)])
+            out[n], lse[n] = o[0], s[0]
+        return out, lse
+    out = np.zeros((T, Hq, D))
+    lse = np.zeros((T, Hq))
+    for b in range(B):
+        ts = list(range(cu[b], cu[b + 1]))
+        if not ts:
+            continue
+        lims = [lim_of(t) for t in ts]
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            o, s = attend_rows(Q[ts[0]:ts[-1] + 1, h], Kc[b, g], Vc[b, g],
+                               None if G is None else G[ts[0]:ts[-1] + 1, h], lims)
+            out[ts[0]:ts[-1] + 1, h] = o
+            lse[ts[0]:ts[-1] + 1, h] = s
+    return out, lse
+
+
+def lse_merge(O_parts, lse_parts, G=None):
+    """Combine S partial results of the same rows over disjoint key sets.
+
+    O_parts [S,N,D]: each part normalised (sum_j p_j V_j / l_s over its keys);
+    lse_parts [S,N]: m_s + ln l_s of the part, -inf for a part with no key.
+    out_n = sum_s exp(lse_s) O_s / sum_s exp(lse_s), times sigmoid(G) when given;
+    lse_n = ln sum_s exp(lse_s).  Parts of weight 0 are not read.  A row whose
+    parts are all empty outputs zeros and lse -inf.
+
+    This is the tail-chunk merge the TensorFold attention contract checks (its
+    control "a merge dropping later tail chunks" must fail).
+    """
+    O_parts = np.asarray(O_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    S, N, D = O_parts.shape
+    out = np.zeros((N, D))
+    lse = np.full(N, -np.inf)
+    for n in range(N):
+        live = [s for s in range(S) if np.isfinite(lse_parts[s, n])]
+        if not live:
+            continue
+        M = max(lse_parts[s, n] for s in live)
+        w = np.array([math.exp(lse_parts[s, n] - M) for s in live])
+        acc = np.zeros(D)
+        for ws, s in zip(w, live):
+            acc += ws * O_parts[s, n]
+        out[n] = acc / w.sum()
+        lse[n] = M + math.log(w.sum())
+    if G is not None:
+        out = out * sigmoid(np.asarray(G, dtype=np.float64).reshape(N, D))
+    return out, lse
+
+
+def head_chunk_plan(rows: int, gqa: int, enabled: bool = True, limit: int = 32):
+    """Head-chunk sizes for one KV group (DS4Server issue113 README, opening
+    rule): when enabled, rows <= 32 and rows*GQA > 32, the group's query heads are
+    split into chunks of min(GQA, 32 // rows) heads with the remainder kept as a
+    last, smaller chunk; otherwise the group is one chunk.  Invalid counts are
+    refused."""
+    if rows < 1 or gqa < 1:
+        raise ValueError("rows and heads per group must be positive")
+    if not enabled or rows > limit or rows * gqa <= limit:
+        return [gqa]
+    c = min(gqa, limit // rows)
+    plan = [c] * (gqa // c)
+    if gqa % c:
+        plan.append(gqa % c)
+    return plan
+
+
+def decode_head_chunked(Q, Kc, Vc, G, kv_lens, cu_rows=None, enabled=True):
+    """Decode/verify evaluated group by group and head chunk by head chunk, then
+    concatenated in head order (DS4Server issue113 README, opening rule).  The
+    method reaches the unchunked result; this exists so that the invariant can be
+    checked."""
+    T, Hq, D = Q.shape
+    B, Hkv = Kc.shape[0], Kc.shape[1]
+    gqa = Hq // Hkv
+    cu = list(range(B + 1)) if cu_rows is None else [int(x) for x in cu_rows]
+    out = np.zeros((T, Hq, D))
+    lse = np.zeros((T, Hq))
+    for b in range(B):
+        r = cu[b + 1] - cu[b]
+        if r == 0:
+            continue
+        sub_cu = [0, r]
+        for g in range(Hkv):
+            h0 = g * gqa
+            for c in head_chunk_plan(r, gqa, enabled):
+                hs = slice(h0, h0 + c)
+                o, s = decode(Q[cu[b]:cu[b + 1], hs], Kc[b:b + 1, g:g + 1], Vc[b:b + 1, g:g + 1],
+                              None if G is None else G[cu[b]:cu[b + 1], hs],
+                              [kv_lens[b]], sub_cu)
+                out[cu[b]:cu[b + 1], hs] = o
+                lse[cu[b]:cu[b + 1], hs] = s
+                h0 += c
+    return out, lse

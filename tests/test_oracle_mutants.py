@@ -1,0 +1,68 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each mutant is the oracle's own source with one plausible mistake typed into it
+(a dropped term, a wrong index or sign, a transposed operand, one key too far, a
+merge that drops a part).  The mutant is built on the CPU as a separate module;
+the test asserts that at least one pin from test_oracle_pins fails on it.
+"""
+import importlib.util
+import os
+import types
+
+import pytest
+
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "attention.py")
+
+MUTANTS = {
+    "one key too far (prefill)": ("return kv_offset + i + 1", "return kv_offset + i + 2"),
+    "one key too far (verify)": ("return kv_len - rows + i + 1", "return kv_len - rows + i + 2"),
+    "one key short (mask compare)": ("np.arange(kmax)[None, :] < lims[:, None]",
+                                     "np.arange(kmax)[None, :] < lims[:, None] - 1"),
+    "wrong scale": ("SCALE = 1.0 / 16.0", "SCALE = 1.0 / 8.0"),
+    "interleaved kv heads": ("return h // (Hq // Hkv)", "return h % Hkv"),
+    "transposed operand (V for K)": ("s = (q_rows @ Kb.T) * SCALE", "s = (q_rows @ Vb.T) * SCALE"),
+    "dropped normalisation": ("o[live] = (p[live] @ Vb) / l[live, None]", "o[live] = (p[live] @ Vb)"),
+    "dropped max shift": ("m = np.where(live, s.max(axis=1), 0.0)", "m = np.where(live, 0.0 * s.max(axis=1), 0.0)"),
+    "gate sign": ("return 1.0 / (1.0 + np.exp(-x))", "return 1.0 / (1.0 + np.exp(x))"),
+    "lse without ln l": ("lse[live] = m[live] + np.log(l[live])", "lse[live] = m[live]"),
+    "merge drops last part": ("live = [s for s in range(S) if np.isfinite(lse_parts[s, n])]",
+                              "live = [s for s in range(S) if np.isfinite(lse_parts[s, n])][:-1]"),
+    "merge ignores weights": ("acc += ws * O_parts[s, n]", "acc += O_parts[s, n]"),
+    "plan drops remainder": ("    if gqa % c:\n        plan.append(gqa % c)\n", ""),
+    "plan chunk one head too wide": ("c = min(gqa, limit // rows)", "c = min(gqa, limit // rows + 1)"),
+    "plan ignores the row bound": ("rows > limit or ", ""),
+}
+
+
+def _build(src, name):
+    mod = types.ModuleType(name)
+    mod.__file__ = SRC
+    exec(compile(src, f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+def test_unmutated_source_passes():
+    with open(SRC) as f:
+        mod = _build(f.read(), "oracle_copy")
+    bad = [c.__name__ for c in pins.CHECKS if c(mod)]
+    assert not bad, bad
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    with open(SRC) as f:
+        src = f.read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site not unique: {old!r}"
+    mod = _build(src.replace(old, new), name)
+    failed = []
+    for c in pins.CHECKS:
+        try:
+            if c(mod):
+                failed.append(c.__name__)
+        except Exception as e:  # a crash also counts as caught
+            failed.append(f"{c.__name__} raised {type(e).__name__}")
+    assert failed, f"no pin caught mutant {name!r}"

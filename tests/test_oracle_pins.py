@@ -1,0 +1,322 @@
+"""Pins for the float64 oracle: checks against things other than the oracle itself.
+
+* brute force in 40-digit arithmetic on tiny inputs (tests/brute.py);
+* a library routine (torch scaled_dot_product_attention in float64, explicit
+  boolean mask, GQA by repeat_interleave);
+* closed forms: one visible key, G = 0 halves the output, a large gate passes it
+  through, equal keys give the mean of the visible values, a dominant score picks
+  its value row;
+* invariants: masked and padded keys never change a row, chunked prefill equals
+  whole prefill, verify rows equal prefill rows at the same positions, head
+  chunks equal the unchunked group, an LSE merge of any key partition equals the
+  unsplit row;
+* the head-chunk plan against the worked example the DS4Server issue113 README
+  prints (tests/golden/head_chunk_plan.txt).
+
+Each check is a function returning an error string (empty when it holds) so that
+test_oracle_mutants.py can run the same checks against oracles with planted
+mistakes.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import make_decode, make_prefill
+from tests import brute
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def _cmp(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.shape != b.shape:
+        return f"{what}: shape {a.shape} vs {b.shape}"
+    if not np.all(np.isfinite(a) == np.isfinite(b)):
+        return f"{what}: finiteness differs"
+    fin = np.isfinite(a)
+    if not fin.any():
+        return ""
+    err = np.max(np.abs(a[fin] - b[fin]) / np.maximum(1.0, np.abs(b[fin])))
+    return "" if err <= tol else f"{what}: max err {err:.3e} > {tol:.1e}"
+
+
+# ---------------------------------------------------------------------------
+# checks (each takes the oracle module so mutants can be substituted)
+# ---------------------------------------------------------------------------
+
+def check_brute_prefill(ora):
+    x = make_prefill(2, 4, 2, 4, Lkv=7, kv_offset=3, seed=11)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    out, lse = ora.prefill(Q, K, V, G, kv_offset=3)
+    ref = brute.prefill(Q, K, V, G, 3)
+    for (b, h, i), (o, l) in ref.items():
+        e = _cmp(out[b, h, i], [float(v) for v in o], 1e-12, f"prefill out {(b, h, i)}")
+        e = e or _cmp(lse[b, h, i], float(l), 1e-12, f"prefill lse {(b, h, i)}")
+        if e:
+            return e
+    return ""
+
+
+def check_brute_prefill_ungated(ora):
+    x = make_prefill(1, 2, 1, 3, seed=12)
+    Q, K, V = (f64(t) for t in (x.q, x.k, x.v))
+    out, _ = ora.prefill(Q, K, V, None, kv_offset=0)
+    ref = brute.prefill(Q, K, V, None, 0)
+    for (b, h, i), (o, _) in ref.items():
+        e = _cmp(out[b, h, i], [float(v) for v in o], 1e-12, f"ungated {(b, h, i)}")
+        if e:
+            return e
+    return ""
+
+
+def check_brute_decode(ora):
+    # ragged rows (0 rows for one sequence), NaN cache padding, GQA 2
+    x = make_decode(3, 4, 2, rows=[1, 0, 3], kv_lens=[5, 2, 6], Lcap=8, seed=13)
+    Q, Kc, Vc, G = (f64(t) for t in (x.q, x.k_cache, x.v_cache, x.g))
+    out, lse = ora.decode(Q, Kc, Vc, G, x.kv_lens.tolist(), x.cu_rows.tolist())
+    ref = brute.decode(Q, Kc, Vc, G, x.kv_lens.tolist(), x.rows)
+    for (t, h), (o, l) in ref.items():
+        e = _cmp(out[t, h], [float(v) for v in o], 1e-12, f"decode out {(t, h)}")
+        e = e or _cmp(lse[t, h], float(l), 1e-12, f"decode lse {(t, h)}")
+        if e:
+            return e
+    return ""
+
+
+def check_library_sdpa(ora):
+    """torch SDPA in float64 with an explicit causal/offset boolean mask."""
+    B, Hq, Hkv, Lq, off = 2, 6, 2, 9, 5
+    x = make_prefill(B, Hq, Hkv, Lq, kv_offset=off, seed=14)
+    q, k, v, g = (t.to(torch.float64) for t in (x.q, x.k, x.v, x.g))
+    Lkv = off + Lq
+    mask = torch.arange(Lkv)[None, :] <= (off + torch.arange(Lq))[:, None]
+    kk = k.repeat_interleave(Hq // Hkv, dim=1)
+    vv = v.repeat_interleave(Hq // Hkv, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=mask,
+                                                           scale=1.0 / 16.0)
+    ref = (ref * torch.sigmoid(g)).numpy()
+    out, _ = ora.prefill(q.numpy(), k.numpy(), v.numpy(), g.numpy(), kv_offset=off)
+    return _cmp(out, ref, 1e-12, "sdpa")
+
+
+def check_one_key(ora):
+    """Lkv = 1: out = V0 * sigmoid(G), lse = the single score."""
+    x = make_prefill(1, 3, 1, 1, seed=15)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    out, lse = ora.prefill(Q, K, V, G, 0)
+    want = V[0, 0, 0][None, :] / (1.0 + np.exp(-G[0, :, 0]))
+    s = (Q[0, :, 0] @ K[0, 0, 0]) / 16.0
+    return _cmp(out[0, :, 0], want, 1e-15, "one key") or _cmp(lse[0, :, 0], s, 1e-15, "one key lse")
+
+
+def check_gate_zero_half(ora):
+    """G = 0: sigmoid(0) = 1/2 exactly, so the output is exactly half the ungated one."""
+    x = make_prefill(1, 4, 2, 6, seed=16)
+    Q, K, V = (f64(t) for t in (x.q, x.k, x.v))
+    gated, _ = ora.prefill(Q, K, V, np.zeros_like(Q), 0)
+    plain, _ = ora.prefill(Q, K, V, None, 0)
+    return "" if np.array_equal(gated, plain * 0.5) else "G=0 is not half"
+
+
+def check_gate_large_passthrough(ora):
+    """G = +40: sigmoid rounds to 1 in float64; G = -40: the output is ~4e-18 of it."""
+    x = make_prefill(1, 4, 2, 6, seed=17)
+    Q, K, V = (f64(t) for t in (x.q, x.k, x.v))
+    plain, _ = ora.prefill(Q, K, V, None, 0)
+    hi, _ = ora.prefill(Q, K, V, np.full_like(Q, 40.0), 0)
+    lo, _ = ora.prefill(Q, K, V, np.full_like(Q, -40.0), 0)
+    e = _cmp(hi, plain, 1e-15, "G=+40")
+    if e:
+        return e
+    return "" if np.max(np.abs(lo)) <= 1e-16 * max(1.0, np.max(np.abs(plain))) else "G=-40 not ~0"
+
+
+def check_equal_keys_mean(ora):
+    """All keys equal: every visible key has the same score, out = mean of the
+    visible V rows times the gate."""
+    x = make_prefill(1, 2, 1, 5, Lkv=8, kv_offset=3, seed=18)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    K[:] = K[:, :, :1]
+    out, _ = ora.prefill(Q, K, V, G, 3)
+    for h in range(2):
+        for i in range(5):
+            want = V[0, 0, :3 + i + 1].mean(axis=0) / (1.0 + np.exp(-G[0, h, i]))
+            e = _cmp(out[0, h, i], want, 1e-14, f"equal keys {(h, i)}")
+            if e:
+                return e
+    return ""
+
+
+def check_dominant_key(ora):
+    """A key whose score exceeds the others by ~1000 (exp would overflow without
+    the max shift) picks its V row exactly."""
+    x = make_prefill(1, 1, 1, 1, Lkv=6, kv_offset=5, seed=19)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    Q[:] = 0.0
+    Q[0, 0, 0, 0] = 16.0 * 1000.0
+    K[:] = 0.0
+    K[0, 0, 3, 0] = 1.0                 # score 1000 for key 3, 0 for the rest
+    out, lse = ora.prefill(Q, K, V, None, 5)
+    e = _cmp(out[0, 0, 0], V[0, 0, 3], 1e-15, "dominant key")
+    return e or _cmp(lse[0, 0, 0], 1000.0, 1e-15, "dominant lse")
+
+
+def check_masked_keys_ignored(ora):
+    """Keys a row does not see (future keys, cache padding) never change it: bit
+    for bit under finite perturbation of future keys and NaN padding."""
+    x = make_prefill(1, 4, 2, 10, Lkv=14, kv_offset=2, seed=20)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    base, _ = ora.prefill(Q, K, V, G, 2)
+    K2, V2 = K.copy(), V.copy()
+    K2[:, :, 8:] += 3.0                 # keys 8..13: rows 0..5 do not see them
+    V2[:, :, 8:] *= -7.0
+    K2[:, :, 12:] = np.nan              # keys 12, 13: no row sees them
+    V2[:, :, 12:] = np.inf
+    pert, _ = ora.prefill(Q, K2, V2, G, 2)
+    if not np.array_equal(base[:, :, :6], pert[:, :, :6]):
+        return "masked future keys changed a row"
+    y = make_decode(2, 4, 2, rows=[2, 1], kv_lens=[5, 3], Lcap=9, seed=21, pad_value=0.0)
+    Qd, Kd, Vd, Gd = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    a, _ = ora.decode(Qd, Kd, Vd, Gd, [5, 3], y.cu_rows.tolist())
+    Kd[0, :, 5:] = np.nan
+    Vd[1, :, 3:] = np.nan
+    b, _ = ora.decode(Qd, Kd, Vd, Gd, [5, 3], y.cu_rows.tolist())
+    return "" if np.array_equal(a, b) else "cache padding changed a row"
+
+
+def check_chunked_prefill(ora):
+    """Any chunking of the prompt rows with kv_offset equals the whole prompt."""
+    x = make_prefill(1, 4, 2, 12, seed=22)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    whole, wl = ora.prefill(Q, K, V, G, 0)
+    for c0, c1 in [(0, 5), (5, 6), (6, 12)]:
+        part, pl = ora.prefill(Q[:, :, c0:c1], K[:, :, :c1], V[:, :, :c1], G[:, :, c0:c1], c0)
+        e = _cmp(part, whole[:, :, c0:c1], 1e-13, f"chunk {c0}:{c1}")
+        e = e or _cmp(pl, wl[:, :, c0:c1], 1e-13, f"chunk lse {c0}:{c1}")
+        if e:
+            return e
+    return ""
+
+
+def check_verify_equals_prefill(ora):
+    """r verify rows at kv_len are prompt rows at kv_offset = kv_len - r."""
+    r, L = 4, 9
+    y = make_decode(1, 4, 2, rows=[r], kv_lens=[L], Lcap=11, seed=23)
+    Qd, Kd, Vd, Gd = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    dec, dl = ora.decode(Qd, Kd, Vd, Gd, [L], [0, r])
+    pre, pl = ora.prefill(Qd.transpose(1, 0, 2)[None], Kd[:, :, :L], Vd[:, :, :L],
+                          Gd.transpose(1, 0, 2)[None], L - r)
+    return (_cmp(dec, pre[0].transpose(1, 0, 2), 1e-13, "verify vs prefill")
+            or _cmp(dl, pl[0].T, 1e-13, "verify vs prefill lse"))
+
+
+def check_head_chunks(ora):
+    """Head-chunked evaluation (chunks of min(GQA, 32/rows), remainder kept) equals
+    the unchunked group.  rows*GQA = 4*12 > 32 gives chunks 8 + 4."""
+    y = make_decode(2, 24, 2, rows=[4, 2], kv_lens=[9, 6], Lcap=10, seed=24)
+    Qd, Kd, Vd, Gd = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    a, al = ora.decode(Qd, Kd, Vd, Gd, [9, 6], y.cu_rows.tolist())
+    b, bl = ora.decode_head_chunked(Qd, Kd, Vd, Gd, [9, 6], y.cu_rows.tolist())
+    return _cmp(b, a, 1e-13, "head chunks") or _cmp(bl, al, 1e-13, "head chunks lse")
+
+
+def check_merge_partition(ora):
+    """An LSE merge of the parts of any key partition equals the unsplit row."""
+    y = make_decode(1, 4, 2, rows=[3], kv_lens=[23], Lcap=23, seed=25)
+    Qd, Kd, Vd, Gd = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    full, fl = ora.decode(Qd, Kd, Vd, Gd, [23], [0, 3])
+    cuts = [0, 4, 5, 13, 21, 30]        # the last part is empty for every row
+    N = 3 * 4
+    parts = np.zeros((len(cuts) - 1, N, 256))
+    lses = np.zeros((len(cuts) - 1, N))
+    for s in range(len(cuts) - 1):
+        a, b = cuts[s], cuts[s + 1]
+        for t in range(3):
+            lim = ora.verify_visible(t, 3, 23)
+            n_keys = max(0, min(b, lim) - a)
+            for h in range(4):
+                g = ora.kv_head_of(h, 4, 2)
+                o, l = ora.attend_rows(Qd[t, h][None], Kd[0, g, a:], Vd[0, g, a:], None, [n_keys])
+                parts[s, t * 4 + h] = o[0]
+                lses[s, t * 4 + h] = l[0]
+    out, lse = ora.lse_merge(parts, lses, Gd.reshape(N, 256))
+    return (_cmp(out, full.reshape(N, 256), 1e-12, "merge")
+            or _cmp(lse, fl.reshape(N), 1e-12, "merge lse"))
+
+
+def check_merge_empty_row(ora):
+    """A row whose parts are all empty is zeros with lse -inf; an empty part among
+    live ones carries weight 0 even when its O holds NaN."""
+    parts = np.zeros((3, 2, 256))
+    parts[1, 1] = np.nan
+    lses = np.array([[-np.inf, 0.5], [-np.inf, -np.inf], [-np.inf, 0.5]])
+    parts[0, 1] = 1.0
+    parts[2, 1] = 3.0
+    out, lse = ora.lse_merge(parts, lses)
+    if not (np.all(out[0] == 0) and lse[0] == -np.inf):
+        return "empty row"
+    e = _cmp(out[1], np.full(256, 2.0), 1e-15, "equal weights")
+    return e or _cmp(lse[1], 0.5 + math.log(2.0), 1e-15, "equal weights lse")
+
+
+def _load_plan_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "head_chunk_plan.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            rows, gqa, plan = line.split(None, 2)
+            cases.append((int(rows), int(gqa), [int(c) for c in plan.split(",")]))
+    return cases
+
+
+def check_plan_golden(ora):
+    for rows, gqa, plan in _load_plan_golden():
+        got = ora.head_chunk_plan(rows, gqa)
+        if got != plan:
+            return f"plan({rows},{gqa}) = {got}, page says {plan}"
+    return ""
+
+
+CHECKS = [
+    check_brute_prefill, check_brute_prefill_ungated, check_brute_decode, check_library_sdpa,
+    check_one_key, check_gate_zero_half, check_gate_large_passthrough, check_equal_keys_mean,
+    check_dominant_key, check_masked_keys_ignored, check_chunked_prefill,
+    check_verify_equals_prefill, check_head_chunks, check_merge_partition,
+    check_merge_empty_row, check_plan_golden,
+]
+
+
+@pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(check):
+    err = check(O)
+    assert not err, err
+
+
+def test_plan_rule_properties():
+    """The plan always covers the group exactly, in order, with chunks <= 32/rows
+    whenever it splits; counts that are not positive are refused."""
+    for rows in range(1, 40):
+        for gqa in range(1, 30):
+            plan = O.head_chunk_plan(rows, gqa)
+            assert sum(plan) == gqa
+            if len(plan) > 1:
+                assert rows * gqa > 32 and rows <= 32
+                assert max(plan) == min(gqa, 32 // rows)
+                assert all(c == plan[0] for c in plan[:-1])
+    for bad in [(0, 4), (4, 0), (-1, 2)]:
+        with pytest.raises(ValueError):
+            O.head_chunk_plan(*bad)
+    assert O.head_chunk_plan(4, 12, enabled=False) == [12]
