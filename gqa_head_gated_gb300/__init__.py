@@ -1,0 +1,168 @@
+"""gqa_head_gated_gb300: gated causal GQA attention at head_dim 256 for GB300.
+
+Thin PyTorch binding over the C ABI of libgqa_attn.so (include/gqa_attn.h).
+It only checks and marshals arguments (pointers, sizes, the current CUDA
+stream) and allocates outputs with torch; every step of the computation runs in
+the library's CUDA kernels.  There is no CPU fallback: without the shared
+library or a CUDA device the calls raise.
+
+    out = softmax(Q K^T / 16 + causal/offset mask) V * sigmoid(G)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import GqaError, check, load  # noqa: F401
+
+HEAD_DIM = 256
+
+__all__ = ["prefill", "decode", "decode_plan", "decode_split", "lse_merge",
+           "decode_workspace_size", "last_device_status", "set_wait_timeout_ns", "GqaError",
+           "load"]
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, ndim, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or t.shape[-1] != HEAD_DIM and ndim >= 3:
+        raise ValueError(f"{name} must be {ndim}-d with last dim {HEAD_DIM}, got {tuple(t.shape)}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def prefill(q, k, v, g=None, kv_offset=0, out=None, return_lse=False):
+    """Prompt rows.  q, g: [B,Hq,Lq,256] bf16; k, v: [B,Hkv,Lkv,256] bf16.
+    Row i sits at position kv_offset + i and sees keys 0..kv_offset+i.
+    Returns out [B,Hq,Lq,256] bf16 (and lse [B,Hq,Lq] fp32 if return_lse)."""
+    _need(q, torch.bfloat16, 4, "q")
+    _need(k, torch.bfloat16, 4, "k")
+    _need(v, torch.bfloat16, 4, "v")
+    if g is not None:
+        _need(g, torch.bfloat16, 4, "g")
+    B, Hq, Lq, _ = q.shape
+    Hkv, Lkv = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device) if return_lse else None
+    code = load().gqa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(lse),
+                                   B, Hq, Hkv, Lq, Lkv, int(kv_offset), _stream())
+    check(code, "gqa_attn_prefill")
+    return (out, lse) if return_lse else out
+
+
+def decode_plan(B, T, Hq, Hkv, max_rows, max_kv_len):
+    """(num_splits, split_keys) that decode() uses for these sizes."""
+    s, c = ctypes.c_int(0), ctypes.c_int(0)
+    check(load().gqa_attn_decode_plan(B, T, Hq, Hkv, max_rows, max_kv_len, ctypes.byref(s),
+                                      ctypes.byref(c)), "gqa_attn_decode_plan")
+    return s.value, c.value
+
+
+def decode_workspace_size(B, T, Hq, Hkv, max_rows, max_kv_len):
+    return int(load().gqa_attn_decode_workspace_size(B, T, Hq, Hkv, max_rows, max_kv_len))
+
+
+def _decode_sizes(q, k_cache, kv_lens, cu_rows, max_rows, max_kv_len):
+    T, Hq, _ = q.shape
+    B, Hkv, Lcap, _ = k_cache.shape
+    if kv_lens.dtype != torch.int32 or not kv_lens.is_cuda or kv_lens.numel() != B:
+        raise ValueError("kv_lens must be an int32 CUDA tensor of B entries")
+    if cu_rows is not None and (cu_rows.dtype != torch.int32 or not cu_rows.is_cuda
+                                or cu_rows.numel() != B + 1):
+        raise ValueError("cu_rows must be an int32 CUDA tensor of B+1 entries")
+    if max_kv_len is None:           # synchronises; pass it to avoid the copy
+        max_kv_len = int(kv_lens.max().item())
+    if max_rows is None:
+        max_rows = 1 if cu_rows is None else int((cu_rows[1:] - cu_rows[:-1]).max().item())
+    return T, Hq, B, Hkv, Lcap, int(max_rows), int(max_kv_len)
+
+
+def decode(q, k_cache, v_cache, g, kv_lens, cu_rows=None, max_rows=None, max_kv_len=None,
+           workspace=None, out=None, return_lse=False):
+    """Decode / chain-verify rows.  q, g: [T,Hq,256] bf16 token-major; caches
+    [B,Hkv,Lcap,256] bf16; kv_lens int32 [B] (counts the new rows); cu_rows int32
+    [B+1] or None (one row per sequence).  Returns out [T,Hq,256] bf16."""
+    _need(q, torch.bfloat16, 3, "q")
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    if g is not None:
+        _need(g, torch.bfloat16, 3, "g")
+    T, Hq, B, Hkv, Lcap, max_rows, max_kv_len = _decode_sizes(q, k_cache, kv_lens, cu_rows,
+                                                               max_rows, max_kv_len)
+    need = decode_workspace_size(B, T, Hq, Hkv, max_rows, max_kv_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if return_lse else None
+    code = load().gqa_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(g), _ptr(kv_lens),
+                                  _ptr(cu_rows), _ptr(out), _ptr(lse), B, T, Hq, Hkv, Lcap,
+                                  max_rows, max_kv_len, _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream())
+    check(code, "gqa_attn_decode")
+    return (out, lse) if return_lse else out
+
+
+def decode_split(q, k_cache, v_cache, kv_lens, cu_rows=None, max_rows=None, max_kv_len=None,
+                 num_splits=None, split_keys=None, o_parts=None, lse_parts=None):
+    """First half of decode: partial results (O/l [S,T*Hq,256] fp32, lse [S,T*Hq])."""
+    _need(q, torch.bfloat16, 3, "q")
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    T, Hq, B, Hkv, Lcap, max_rows, max_kv_len = _decode_sizes(q, k_cache, kv_lens, cu_rows,
+                                                               max_rows, max_kv_len)
+    if num_splits is None or split_keys is None:
+        num_splits, split_keys = decode_plan(B, T, Hq, Hkv, max_rows, max_kv_len)
+    if o_parts is None:
+        o_parts = torch.empty((num_splits, T * Hq, HEAD_DIM), dtype=torch.float32, device=q.device)
+    if lse_parts is None:
+        lse_parts = torch.empty((num_splits, T * Hq), dtype=torch.float32, device=q.device)
+    code = load().gqa_attn_decode_split(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_lens),
+                                        _ptr(cu_rows), _ptr(o_parts), _ptr(lse_parts), B, T, Hq,
+                                        Hkv, Lcap, max_rows, max_kv_len, num_splits, split_keys,
+                                        _stream())
+    check(code, "gqa_attn_decode_split")
+    return o_parts, lse_parts
+
+
+def lse_merge(o_parts, lse_parts, g=None, out=None, return_lse=False):
+    """Merge S partial results: o_parts [S,N,256] fp32, lse_parts [S,N] fp32,
+    g None or [N,256] bf16 (any shape with N*256 elements).  Returns out [N,256] bf16."""
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise TypeError("o_parts and lse_parts must be float32")
+    if not (o_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("o_parts and lse_parts must be contiguous CUDA tensors")
+    S, N, D = o_parts.shape
+    if D != HEAD_DIM or tuple(lse_parts.shape) != (S, N):
+        raise ValueError("shapes must be [S,N,256] and [S,N]")
+    if g is not None and (g.dtype != torch.bfloat16 or g.numel() != N * HEAD_DIM
+                          or not g.is_contiguous()):
+        raise ValueError("g must be contiguous bf16 with N*256 elements")
+    if out is None:
+        out = torch.empty((N, HEAD_DIM), dtype=torch.bfloat16, device=o_parts.device)
+    lse = torch.empty(N, dtype=torch.float32, device=o_parts.device) if return_lse else None
+    code = load().attn_lse_merge(_ptr(o_parts), _ptr(lse_parts), S, N, _ptr(g), _ptr(out),
+                                 _ptr(lse), _stream())
+    check(code, "attn_lse_merge")
+    return (out, lse) if return_lse else out
+
+
+def last_device_status():
+    """Synchronises the current stream; returns and clears the device status code."""
+    return load().gqa_last_device_status(_stream())
+
+
+def set_wait_timeout_ns(ns):
+    load().gqa_set_wait_timeout_ns(int(ns))

@@ -1,0 +1,256 @@
+// C ABI of libgqa_attn.so: argument validation, split planning, the device
+// status word, and the launches.  The operation and conventions are stated in
+// include/gqa_attn.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "gqa_attn.h"
+#include "internal.h"
+
+namespace gqa {
+namespace {
+
+__device__ int g_status_word;
+
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultSMs = 152;   // GB300
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device address of the status word on the current device (looked up once per device).
+int* status_ptr() {
+  static std::mutex mu;
+  static int* ptrs[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static int counts[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kDefaultSMs;
+  std::lock_guard<std::mutex> lock(mu);
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = kDefaultSMs;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+bool make_ctl(LaunchCtl* ctl) {
+  ctl->status = status_ptr();
+  ctl->timeout_ns = g_timeout_ns.load();
+  return ctl->status != nullptr;
+}
+
+int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
+
+// Decode split plan: aim for about four CTAs per SM over the (sequence, group,
+// row block) units, with splits of whole 64-key steps.
+int plan_decode(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int num_sms, int* S,
+                int* C) {
+  const int gqa = Hq / Hkv;
+  const long long packed = (long long)max_rows * gqa;
+  const int MB = decode_rows_per_cta(int(packed > (1 << 30) ? (1 << 30) : packed));
+  const long long n_rb = (packed + MB - 1) / MB;
+  const long long units = (long long)B * Hkv * n_rb;
+  const long long want = 4LL * num_sms;
+  long long s = (want + units - 1) / units;
+  const long long steps = (max_kv_len + 63) / 64;
+  if (s > steps) s = steps;
+  if (s < 1) s = 1;
+  long long c = ((max_kv_len + s - 1) / s + 63) / 64 * 64;
+  s = (max_kv_len + c - 1) / c;
+  *S = int(s);
+  *C = int(c);
+  return GQA_OK;
+}
+
+int check_decode_args(int B, int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                      bool has_cu_rows) {
+  if (B < 1 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lcap < 1) return GQA_ERR_INVALID_ARG;
+  if (max_rows < 1 || max_kv_len < 1 || max_kv_len > Lcap || max_rows > max_kv_len)
+    return GQA_ERR_INVALID_ARG;
+  if (!has_cu_rows && (T != B || max_rows != 1)) return GQA_ERR_INVALID_ARG;
+  if ((long long)T > (long long)B * max_rows) return GQA_ERR_INVALID_ARG;
+  if ((long long)T * Hq >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv * Lcap >= (1LL << 40)) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+size_t workspace_bytes_for(int T, int Hq, int S) {
+  const size_t rows = size_t(T) * size_t(Hq);
+  return size_t(S) * rows * 256 * sizeof(float) + size_t(S) * rows * sizeof(float);
+}
+
+int run_split(const void* Q, const void* Kc, const void* Vc, const int* kv_lens,
+              const int* cu_rows, float* O_parts, float* lse_parts, int B, int T, int Hq, int Hkv,
+              int Lcap, int max_rows, int max_kv_len, int S, int C, cudaStream_t stream) {
+  LaunchCtl ctl;
+  if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
+  DecodeSplitArgs a{Q, Kc, Vc, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
+                    max_rows, max_kv_len, S, C};
+  return launch_decode_split(a, ctl, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" {
+
+const char* gqa_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GQA_ERR_CUDA: return "CUDA error";
+    case GQA_ERR_TIMEOUT: return "device wait timed out";
+    case GQA_ERR_WORKSPACE: return "workspace too small";
+    case GQA_ERR_DEVICE_RANGE: return "device-side range error (kv_lens / cu_rows)";
+    default: return "unknown status";
+  }
+}
+
+const char* gqa_version(void) { return "0.1.0"; }
+
+void gqa_set_wait_timeout_ns(unsigned long long ns) {
+  g_timeout_ns.store(ns < 1000000ull ? 1000000ull : ns);
+}
+
+int gqa_attn_prefill(const void* Q, const void* K, const void* V, const void* G, void* out,
+                     float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv, int kv_offset,
+                     gqa_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq < 0 || Lkv < 1 || kv_offset < 0 ||
+      (long long)kv_offset + Lq > Lkv)
+    return GQA_ERR_INVALID_ARG;
+  if (Q == nullptr || K == nullptr || V == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 16) ||
+      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)))
+    return GQA_ERR_INVALID_ARG;
+  if (Hq / Hkv > 128) return GQA_ERR_UNSUPPORTED;
+  if ((long long)Hq * Lq >= (1LL << 31) || (long long)B * Hkv >= (1LL << 31))
+    return GQA_ERR_UNSUPPORTED;
+  if (Lq == 0) return GQA_OK;
+  const long long grid = (long long)ceil_div(Lq, prefill_rows_per_tile(Hq / Hkv)) * B * Hkv;
+  if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
+  LaunchCtl ctl;
+  if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
+  PrefillArgs a{Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset};
+  bool encode_failed = false;
+  const cudaError_t e = launch_prefill(a, ctl, static_cast<cudaStream_t>(stream), &encode_failed);
+  if (encode_failed) return GQA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+int gqa_attn_decode_plan(int B, int T, int Hq, int Hkv, int max_rows, int max_kv_len,
+                         int* num_splits, int* split_keys) {
+  if (num_splits == nullptr || split_keys == nullptr) return GQA_ERR_INVALID_ARG;
+  const int st = check_decode_args(B, T, Hq, Hkv, max_kv_len, max_rows, max_kv_len, true);
+  if (st != GQA_OK) return st;
+  return plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), num_splits, split_keys);
+}
+
+size_t gqa_attn_decode_workspace_size(int B, int T, int Hq, int Hkv, int max_rows,
+                                      int max_kv_len) {
+  int S = 0, C = 0;
+  if (gqa_attn_decode_plan(B, T, Hq, Hkv, max_rows, max_kv_len, &S, &C) != GQA_OK) return 0;
+  return workspace_bytes_for(T, Hq, S);
+}
+
+int gqa_attn_decode_split(const void* Q, const void* Kcache, const void* Vcache,
+                          const int* kv_lens, const int* cu_rows, float* O_parts,
+                          float* lse_parts, int B, int T, int Hq, int Hkv, int Lcap, int max_rows,
+                          int max_kv_len, int num_splits, int split_keys, gqa_stream_t stream) {
+  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
+  if (st != GQA_OK) return st;
+  if (num_splits < 1 || split_keys < 64 || split_keys % 64 != 0 ||
+      (long long)num_splits * split_keys < max_kv_len)
+    return GQA_ERR_INVALID_ARG;
+  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
+      O_parts == nullptr || lse_parts == nullptr)
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(O_parts, 16) ||
+      !aligned(lse_parts, 4) || !aligned(kv_lens, 4) || (cu_rows && !aligned(cu_rows, 4)))
+    return GQA_ERR_INVALID_ARG;
+  if (T == 0) return GQA_OK;
+  const int gqa = Hq / Hkv;
+  const long long packed = (long long)max_rows * gqa;
+  const int MB = decode_rows_per_cta(int(packed > (1 << 30) ? (1 << 30) : packed));
+  const long long grid = (long long)B * Hkv * num_splits * ((packed + MB - 1) / MB);
+  if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
+  return run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
+                   max_rows, max_kv_len, num_splits, split_keys,
+                   static_cast<cudaStream_t>(stream));
+}
+
+int attn_lse_merge(const float* O_parts, const float* lse_parts, int S, int N, const void* G,
+                   void* out, float* lse_out, gqa_stream_t stream) {
+  if (S < 1 || N < 0) return GQA_ERR_INVALID_ARG;
+  if (N == 0) return GQA_OK;
+  if (O_parts == nullptr || lse_parts == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
+  if (!aligned(O_parts, 16) || !aligned(lse_parts, 4) || !aligned(out, 16) ||
+      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)))
+    return GQA_ERR_INVALID_ARG;
+  LaunchCtl ctl;
+  if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
+  MergeArgs a{O_parts, lse_parts, S, N, G, out, lse_out};
+  return launch_lse_merge(a, ctl, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+int gqa_attn_decode(const void* Q, const void* Kcache, const void* Vcache, const void* G,
+                    const int* kv_lens, const int* cu_rows, void* out, float* lse_out, int B,
+                    int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                    void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
+  if (st != GQA_OK) return st;
+  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
+      out == nullptr)
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || (G != nullptr && !aligned(G, 16)) ||
+      (lse_out != nullptr && !aligned(lse_out, 4)))
+    return GQA_ERR_INVALID_ARG;
+  if (T == 0) return GQA_OK;
+  int S = 0, C = 0;
+  plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
+  const size_t need = workspace_bytes_for(T, Hq, S);
+  if (workspace == nullptr || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return GQA_ERR_INVALID_ARG;
+  float* O_parts = static_cast<float*>(workspace);
+  float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
+  int r = gqa_attn_decode_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq,
+                                Hkv, Lcap, max_rows, max_kv_len, S, C, stream);
+  if (r != GQA_OK) return r;
+  return attn_lse_merge(O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
+}
+
+int gqa_last_device_status(gqa_stream_t stream) {
+  int* p = status_ptr();
+  if (p == nullptr) return GQA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess) return GQA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GQA_ERR_CUDA;
+  return v;
+}
+
+}  // extern "C"

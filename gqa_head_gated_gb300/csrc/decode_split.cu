@@ -1,0 +1,406 @@
+// Decode / chain-verify split kernel: for one (sequence b, KV group g, key split s,
+// row block), the attention of the group's query heads x new rows over the split's
+// keys, written as a normalised partial result (O/l, m + ln l) for the LSE merge.
+//
+// The method (TensorFold PR #1009, "Receipt", attention contract paragraph)
+// runs decode over fixed-size cache chunks and merges their partial results; here
+// a split is `split_keys` keys and the merge is attn_lse_merge.  All query heads
+// of a KV group are packed with the rows into the MMA M dimension (packed row
+// p = row * GQA + head), so every K/V byte is read once per split for the whole
+// group (DS4Server issue113 README, opening rule).
+//
+// Memory-bound: K/V tiles of 32 keys (32 KB for K+V) stream through a 4-stage
+// cp.async ring with 16-byte vector copies, coalesced along the 512-byte rows;
+// rows at or past the split's end are zero-filled by the copy itself, so cache
+// padding is never read.  Scores and P.V run on bf16 mma.sync (m16n8k16,
+// fp32 accumulate); the online softmax is fp32 with quad-shuffle row reductions.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace gqa {
+namespace {
+
+constexpr int kTK = 32;          // keys per tile
+constexpr int kStages = 4;
+constexpr int kThreads = 128;
+constexpr int kRowBytes = 512;   // 256 bf16
+constexpr int kTileBytes = kTK * kRowBytes;   // one of K or V
+
+struct Params {
+  const __nv_bfloat16* Q;
+  const __nv_bfloat16* K;
+  const __nv_bfloat16* V;
+  const int* kv_lens;
+  const int* cu_rows;
+  float* O_parts;
+  float* lse_parts;
+  int B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, gqa, split_keys, num_splits, n_rb;
+  LaunchCtl ctl;
+};
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy; src_bytes = 0 zero-fills without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Byte offset of 16-byte chunk `c` (0..31) of row `r` in a 512-byte-row tile:
+// chunks are XOR-swizzled by the row's low 3 bits so ldmatrix is conflict-free.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return uint32_t(r) * kRowBytes + uint32_t((c ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// WR row groups of 16 packed rows; WK key groups per row group (WR * WK warps).
+template <int WR, int WK>
+__global__ void __launch_bounds__(kThreads)
+decode_split_kernel(const Params p) {
+  constexpr int MB = 16 * WR;          // packed rows per CTA
+  constexpr int NK = kTK / WK;         // keys per warp per tile
+  constexpr int NT = NK / 8;           // score n-tiles per warp
+  static_assert(WR * WK <= kThreads / 32, "too many warps");
+  static_assert(NK % 16 == 0, "a warp needs whole k16 steps of P.V");
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sQ = smem;                                    // MB x 512 B
+  uint8_t* sKV = smem + MB * kRowBytes;                  // kStages x (K tile, V tile)
+  __shared__ float s_m[WK][MB];
+  __shared__ float s_l[WK][MB];
+  __shared__ int s_lim[MB];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  int bid = blockIdx.x;
+  const int rb = bid % p.n_rb;
+  bid /= p.n_rb;
+  const int s = bid % p.num_splits;
+  bid /= p.num_splits;
+  const int g = bid % p.Hkv;
+  const int b = bid / p.Hkv;
+
+  const int kv_len = p.kv_lens[b];
+  const int t0 = p.cu_rows ? p.cu_rows[b] : b;
+  const int t1 = p.cu_rows ? p.cu_rows[b + 1] : b + 1;
+  const int rows = t1 - t0;
+  if (rows < 0 || rows > p.max_rows || t1 > p.T || t0 < 0 || kv_len > p.max_kv_len ||
+      kv_len > p.Lcap || kv_len < rows) {
+    if (tid == 0 && rb == 0 && s == 0 && g == 0) record_status(p.ctl.status, GQA_ERR_DEVICE_RANGE);
+    return;
+  }
+  const int P = rows * p.gqa;                 // packed rows of this (b, g)
+  const int p0 = rb * MB;
+  if (p0 >= P) return;                        // row block past this sequence's rows
+  const int k_lo = s * p.split_keys;
+  const int k_hi = min(k_lo + p.split_keys, kv_len);
+
+  // Visible keys of each packed row of the block (0 for padding rows).
+  if (tid < MB) {
+    const int pp = p0 + tid;
+    int lim = 0;
+    if (pp < P) lim = kv_len - rows + pp / p.gqa + 1;
+    s_lim[tid] = min(lim, k_hi);
+  }
+  int n_hi = 0;   // keys any row of the block sees in this split
+  {
+    const int pl = min(P - 1, p0 + MB - 1);
+    n_hi = min(kv_len - rows + pl / p.gqa + 1, k_hi);
+  }
+  const int n_tiles = n_hi > k_lo ? (n_hi - k_lo + kTK - 1) / kTK : 0;
+
+  const size_t kv_base = (size_t(b) * p.Hkv + g) * size_t(p.Lcap) * 256;
+  const __nv_bfloat16* Kg = p.K + kv_base;
+  const __nv_bfloat16* Vg = p.V + kv_base;
+
+  // Q block: packed row pp -> token t0 + pp / gqa, head g*gqa + pp % gqa.
+  {
+    const uint32_t q0 = saddr(sQ);
+    for (int c = tid; c < MB * 32; c += kThreads) {
+      const int r = c >> 5, ch = c & 31;
+      const int pp = p0 + r;
+      const bool ok = pp < P;
+      const __nv_bfloat16* src =
+          ok ? p.Q + ((size_t(t0 + pp / p.gqa) * p.Hq) + g * p.gqa + pp % p.gqa) * 256 + ch * 8
+             : p.Q;
+      cp_async16(q0 + swz(r, ch), src, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  }
+  auto load_tile = [&](int tile, int stage) {
+    const int key0 = k_lo + tile * kTK;
+    const uint32_t kd = saddr(sKV + stage * 2 * kTileBytes);
+    const uint32_t vd = kd + kTileBytes;
+#pragma unroll
+    for (int i = 0; i < (kTK * 32) / kThreads; ++i) {
+      const int c = tid + i * kThreads;
+      const int r = c >> 5, ch = c & 31;
+      const int key = key0 + r;
+      const bool ok = key < n_hi;
+      const size_t off = ok ? size_t(key) * 256 + ch * 8 : 0;
+      cp_async16(kd + swz(r, ch), Kg + off, ok ? 16u : 0u);
+      cp_async16(vd + swz(r, ch), Vg + off, ok ? 16u : 0u);
+    }
+  };
+#pragma unroll
+  for (int st = 0; st < kStages - 1; ++st) {
+    if (st < n_tiles) load_tile(st, st);
+    cp_async_commit();
+  }
+
+  const int wr = warp / WK;
+  const int wk = warp % WK;
+  const bool compute = warp < WR * WK;
+  const int g4 = lane >> 2;       // row within the 8-row half of the fragment
+  const int t4 = lane & 3;
+
+  float o[32][4];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m_r[2] = {-INFINITY, -INFINITY};
+  float l_r[2] = {0.f, 0.f};
+
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    {
+      const int nt = tile + kStages - 1;
+      if (nt < n_tiles) load_tile(nt, nt % kStages);
+      cp_async_commit();
+    }
+    if (!compute) continue;
+    const int stage = tile % kStages;
+    const uint32_t kb = saddr(sKV + stage * 2 * kTileBytes);
+    const uint32_t vb = kb + kTileBytes;
+    const uint32_t qb = saddr(sQ);
+
+    // S = Q K^T over this warp's NK keys.
+    float sc[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      {
+        const int r = wr * 16 + (lane & 15);
+        const int ch = 2 * kk + (lane >> 4);
+        ldsm_x4(qb + swz(r, ch), a0, a1, a2, a3);
+      }
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {
+        uint32_t b0, b1, b2, b3;
+        const int r = wk * NK + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int ch = 2 * kk + ((lane >> 3) & 1);
+        ldsm_x4(kb + swz(r, ch), b0, b1, b2, b3);
+        mma_bf16(sc[2 * np], a0, a1, a2, a3, b0, b1);
+        mma_bf16(sc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    // Mask, online softmax (two rows per thread: g4 and g4 + 8).
+    const int key_w = k_lo + tile * kTK + wk * NK;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int lim = s_lim[wr * 16 + g4 + 8 * hr];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = key_w + nt * 8 + 2 * t4 + e;
+          float v = sc[nt][2 * hr + e];
+          v = key < lim ? v * kScaleLog2 : -INFINITY;
+          sc[nt][2 * hr + e] = v;
+          mx = fmaxf(mx, v);
+        }
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_r[hr], mx);
+      const float msub = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2(m_r[hr] - msub);   // 0 when nothing was seen before
+      m_r[hr] = m_new;
+      float ls = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float pv = ex2(sc[nt][2 * hr + e] - msub);
+          sc[nt][2 * hr + e] = pv;
+          ls += pv;
+        }
+      }
+      l_r[hr] = l_r[hr] * alpha + ls;
+#pragma unroll
+      for (int dn = 0; dn < 32; ++dn) {
+        o[dn][2 * hr] *= alpha;
+        o[dn][2 * hr + 1] *= alpha;
+      }
+    }
+    // O += P V over this warp's keys.
+#pragma unroll
+    for (int ks = 0; ks < NK / 16; ++ks) {
+      const uint32_t pa0 = pack_bf16x2(sc[2 * ks][0], sc[2 * ks][1]);
+      const uint32_t pa1 = pack_bf16x2(sc[2 * ks][2], sc[2 * ks][3]);
+      const uint32_t pa2 = pack_bf16x2(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+      const uint32_t pa3 = pack_bf16x2(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+      const int r = wk * NK + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+      for (int dp = 0; dp < 16; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        const int ch = 2 * dp + (lane >> 4);
+        ldsm_x4_t(vb + swz(r, ch), b0, b1, b2, b3);
+        mma_bf16(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
+        mma_bf16(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // Combine the key groups of each row block in shared memory, then write the
+  // normalised part.  Reuses the K/V ring: WK x MB x 256 fp32 <= 64 KB.
+  float* sO = reinterpret_cast<float*>(sKV);
+  if (compute) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float l = l_r[hr];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      const int r = wr * 16 + g4 + 8 * hr;
+      if (t4 == 0) {
+        s_m[wk][r] = m_r[hr];
+        s_l[wk][r] = l;
+      }
+      float* dst = sO + (size_t(wk) * MB + r) * 256;
+#pragma unroll
+      for (int dn = 0; dn < 32; ++dn)
+        *reinterpret_cast<float2*>(dst + dn * 8 + 2 * t4) = make_float2(o[dn][2 * hr], o[dn][2 * hr + 1]);
+    }
+  }
+  __syncthreads();
+  const int rows_blk = min(MB, P - p0);
+  for (int idx = tid; idx < rows_blk * 64; idx += kThreads) {
+    const int r = idx >> 6;
+    const int c4 = (idx & 63) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < WK; ++k) M = fmaxf(M, s_m[k][r]);
+    const int pp = p0 + r;
+    const size_t n = size_t(t0 + pp / p.gqa) * p.Hq + g * p.gqa + pp % p.gqa;
+    const size_t part = size_t(s) * size_t(p.T) * p.Hq + n;
+    if (M == -INFINITY) {
+      if (c4 == 0) p.lse_parts[part] = -INFINITY;
+      continue;
+    }
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < WK; ++k) {
+      const float w = ex2(s_m[k][r] - M);
+      L += w * s_l[k][r];
+      const float4 v = *reinterpret_cast<const float4*>(sO + (size_t(k) * MB + r) * 256 + c4);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    const float inv = 1.f / L;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    *reinterpret_cast<float4*>(p.O_parts + part * 256 + c4) = acc;
+    if (c4 == 0) p.lse_parts[part] = (M + __log2f(L)) * kLn2;
+  }
+}
+
+template <int WR, int WK>
+cudaError_t launch_t(const Params& p, cudaStream_t stream, long long grid) {
+  constexpr int MB = 16 * WR;
+  const size_t smem = size_t(MB) * kRowBytes + size_t(kStages) * 2 * kTileBytes;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<WR, WK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  decode_split_kernel<WR, WK><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_rows_per_cta(int packed_rows) {
+  if (packed_rows <= 16) return 16;
+  if (packed_rows <= 32) return 32;
+  return 64;
+}
+
+cudaError_t launch_decode_split(const DecodeSplitArgs& a, const LaunchCtl& ctl,
+                                cudaStream_t stream) {
+  Params p;
+  p.Q = static_cast<const __nv_bfloat16*>(a.Q);
+  p.K = static_cast<const __nv_bfloat16*>(a.K);
+  p.V = static_cast<const __nv_bfloat16*>(a.V);
+  p.kv_lens = a.kv_lens;
+  p.cu_rows = a.cu_rows;
+  p.O_parts = a.O_parts;
+  p.lse_parts = a.lse_parts;
+  p.B = a.B;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Lcap = a.Lcap;
+  p.max_rows = a.max_rows;
+  p.max_kv_len = a.max_kv_len;
+  p.gqa = a.Hq / a.Hkv;
+  p.split_keys = a.split_keys;
+  p.num_splits = a.num_splits;
+  p.ctl = ctl;
+  const int MB = decode_rows_per_cta(a.max_rows * p.gqa);
+  p.n_rb = (a.max_rows * p.gqa + MB - 1) / MB;
+  const long long grid = (long long)a.B * a.Hkv * a.num_splits * p.n_rb;
+  if (MB == 16) return launch_t<1, 2>(p, stream, grid);
+  if (MB == 32) return launch_t<2, 2>(p, stream, grid);
+  return launch_t<4, 1>(p, stream, grid);
+}
+
+}  // namespace gqa

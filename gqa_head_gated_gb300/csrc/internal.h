@@ -1,0 +1,58 @@
+// Host-side launchers shared between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+
+namespace gqa {
+
+struct PrefillArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* G;
+  void* out;
+  float* lse;
+  int B, Hq, Hkv, Lq, Lkv, kv_offset;
+};
+
+// Rows of one prefill tile: floor(128 / GQA) query rows of every head in the group.
+inline int prefill_rows_per_tile(int gqa) { return 128 / gqa; }
+
+// Returns cudaSuccess, or the error of encoding the tensor maps / launching.
+// Sets *encode_failed when a TMA descriptor could not be built.
+cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStream_t stream,
+                           bool* encode_failed);
+
+struct DecodeSplitArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const int* kv_lens;
+  const int* cu_rows;
+  float* O_parts;
+  float* lse_parts;
+  int B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, num_splits, split_keys;
+};
+
+// Packed query rows (heads x rows of one KV group) per decode CTA: 16, 32 or 64.
+int decode_rows_per_cta(int packed_rows);
+
+cudaError_t launch_decode_split(const DecodeSplitArgs& a, const LaunchCtl& ctl,
+                                cudaStream_t stream);
+
+struct MergeArgs {
+  const float* O_parts;
+  const float* lse_parts;
+  int S, N;
+  const void* G;
+  void* out;
+  float* lse_out;
+};
+
+cudaError_t launch_lse_merge(const MergeArgs& a, const LaunchCtl& ctl, cudaStream_t stream);
+
+}  // namespace gqa

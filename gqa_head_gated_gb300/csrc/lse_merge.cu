@@ -1,0 +1,94 @@
+// attn_lse_merge: combine S partial attention results of the same rows computed
+// over disjoint key sets, then apply the sigmoid output gate and round to bf16.
+//
+//   out[n,:] = sum_s exp(lse_s - M) O_s[n,:] / sum_s exp(lse_s - M) * sigmoid(G[n,:])
+//   lse[n]   = M + ln sum_s exp(lse_s - M),   M = max_s lse_s
+//
+// This is the tail-chunk merge of the TensorFold PR #1009 attention contract
+// ("Receipt": decode over cache chunks, then a merge; its control "a merge
+// dropping later tail chunks" must fail).  Parts with lse = -inf carry weight 0
+// and their O rows are never read.  One warp per row; each lane owns 8 of the
+// 256 columns and reads them as two float4 per part.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace gqa {
+namespace {
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32)
+lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ lse_parts, int S,
+                 int N, const __nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__ out,
+                 float* __restrict__ lse_out) {
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (n >= N) return;
+  const size_t stride = size_t(N);
+
+  float M = -INFINITY;
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse_parts + size_t(s) * stride + n));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  const int c0 = lane * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      const float ls = __ldg(lse_parts + size_t(s) * stride + n);
+      if (ls == -INFINITY) continue;
+      const float w = __expf(ls - M);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(O_parts + (size_t(s) * stride + n) * 256 + c0);
+      const float4 a = __ldg(src);
+      const float4 b = __ldg(src + 1);
+      acc[0] += w * a.x;
+      acc[1] += w * a.y;
+      acc[2] += w * a.z;
+      acc[3] += w * a.w;
+      acc[4] += w * b.x;
+      acc[5] += w * b.y;
+      acc[6] += w * b.z;
+      acc[7] += w * b.w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  float gs[8];
+  if (G != nullptr) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(G + size_t(n) * 256 + c0));
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(w4[e]);
+      gs[2 * e] = gate_sigmoid(f.x);
+      gs[2 * e + 1] = gate_sigmoid(f.y);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) gs[e] = 1.f;
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0] * inv * gs[0], acc[1] * inv * gs[1]);
+  o.y = pack_bf16x2(acc[2] * inv * gs[2], acc[3] * inv * gs[3]);
+  o.z = pack_bf16x2(acc[4] * inv * gs[4], acc[5] * inv * gs[5]);
+  o.w = pack_bf16x2(acc[6] * inv * gs[6], acc[7] * inv * gs[7]);
+  *reinterpret_cast<uint4*>(out + size_t(n) * 256 + c0) = o;
+  if (lse_out != nullptr && lane == 0)
+    lse_out[n] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(const MergeArgs& a, const LaunchCtl& ctl, cudaStream_t stream) {
+  (void)ctl;
+  const long long grid = (a.N + kWarps - 1) / kWarps;
+  lse_merge_kernel<<<dim3(unsigned(grid)), dim3(kWarps * 32), 0, stream>>>(
+      a.O_parts, a.lse_parts, a.S, a.N, static_cast<const __nv_bfloat16*>(a.G),
+      static_cast<__nv_bfloat16*>(a.out), a.lse_out);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

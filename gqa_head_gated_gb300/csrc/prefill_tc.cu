@@ -1,0 +1,494 @@
+// Prefill (prompt rows) of gated causal GQA attention on sm_103a tensor cores.
+//
+// One CTA computes one tile of 128 packed rows: R = floor(128/GQA) consecutive
+// query rows of every query head of one KV group (row m of the tile is head
+// m / R, query row r0 + m % R), so each K/V tile staged in shared memory serves
+// the whole group (DS4Server issue113 README, opening rule: the heads of a KV
+// group share its K/V).  Rows past R*GQA are padding and are never stored.
+//
+// Roles (320 threads):
+//   warp 0      TMA producer: Q tile once, then K_0, K_1, V_0, K_2, V_1, ... into a
+//               2-slot ring of 64 KB tiles (128 keys x 256 dims, 128-byte swizzle).
+//   warp 1      TMEM allocator and MMA issuer (one thread):
+//                 S_j = Q K_j^T          M=128, N=128, K=256, A and B from smem
+//                 O  += P_j V_j          M=128, N=256, K=128, A (P) from TMEM
+//               in the order S_0, S_1, PV_0, S_2, PV_1, ..., so the tensor pipe
+//               works on S_{j+1} while the softmax runs on S_j.
+//   warps 2..9  softmax and epilogue; TMEM lane = tile row, so a thread owns a row
+//               and a pair of warps (w, w+4) shares its lanes: the first takes keys
+//               0..63 of the tile, the second 64..127; the two exchange row maxima
+//               and sums through shared memory.
+// TMEM (512 columns): O at 0..255 (fp32), S double buffer at 256..383 / 384..511;
+// P_j is written as bf16 pairs over the first 32 columns of each half of S_j.
+//
+// Softmax: fp32, base 2 with the 1/16 scale folded in; the running max is only
+// moved (and O rescaled) when a tile raises it by more than 8 (a factor 256),
+// so p <= 256 and fp32 sums stay exact enough.  Masked keys get probability
+// exactly 0 by selection, never exp(-inf)*0 arithmetic; K/V rows past the last
+// row's horizon are zero-filled by TMA, so nothing outside the visible range is
+// ever multiplied.  Epilogue: out = O / l * sigmoid(G), rounded once to bf16.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx_sm100.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kM = 128;                       // packed rows per tile
+constexpr int kN = 128;                       // keys per K/V tile
+constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle column)
+constexpr int kTileBytes = 4 * kChunkBytes;   // 128 rows x 256 bf16
+constexpr int kSlots = 2;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmO = 0;
+constexpr uint32_t kTmS = 256;                // S buffer b at kTmS + 128*b
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+
+constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kM, kN, 0, 0);    // Q, K both K-major
+constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kM, 256, 0, 1);  // V is MN-major
+
+struct __align__(1024) Smem {
+  uint8_t q[kTileBytes];
+  uint8_t kv[kSlots][kTileBytes];
+  uint64_t q_full;
+  uint64_t kv_full[kSlots];
+  uint64_t kv_empty[kSlots];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done;
+  uint64_t o_final;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int zero;
+  float red[2][2][kM];     // [tile parity][half][row]: row maxima, then row sums
+  int ok[2][2][kM];        // [tile parity][half][row]: the thread's waits succeeded
+};
+
+struct Params {
+  const __nv_bfloat16* G;
+  __nv_bfloat16* out;
+  float* lse;
+  int B, Hq, Hkv, Lq, kv_offset, gqa, R, n_rtiles;
+  LaunchCtl ctl;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+__device__ __forceinline__ void fail(Smem& sm, const Params& p) {
+  sm.abort = 1;
+  record_status(p.ctl.status, GQA_ERR_TIMEOUT);
+}
+
+// Item `it` of the load / consume sequence K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}.
+__device__ __forceinline__ void item_kind(int it, int n, bool& is_v, int& j) {
+  if (it == 0) {
+    is_v = false; j = 0;
+  } else if (it == 2 * n - 1) {
+    is_v = true; j = n - 1;
+  } else {
+    const int m = (it - 1) >> 1;
+    is_v = ((it - 1) & 1) != 0;
+    j = is_v ? m : m + 1;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int BH = p.B * p.Hkv;
+  const int rt = p.n_rtiles - 1 - static_cast<int>(blockIdx.x) / BH;   // longest first
+  const int bg = static_cast<int>(blockIdx.x) % BH;
+  const int b = bg / p.Hkv;
+  const int g = bg % p.Hkv;
+  const int r0 = rt * p.R;
+  const int rows_here = min(p.R, p.Lq - r0);
+  const int n_keys = p.kv_offset + r0 + rows_here;   // keys the last row of the tile sees
+  const int n_tiles = (n_keys + kN - 1) / kN;
+  const uint64_t tmo = p.ctl.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kSlots; ++s) {
+      ptx::mbar_init(&sm.kv_full[s], 1);
+      ptx::mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&sm.s_full[s], 1);
+      ptx::mbar_init(&sm.p_full[s], 8);
+    }
+    ptx::mbar_init(&sm.pv_done, 1);
+    ptx::mbar_init(&sm.o_final, 1);
+    ptx::mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    sm.zero = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+      const uint32_t q_bytes = 4u * 128u * uint32_t(p.R * p.gqa);
+      ptx::mbar_arrive_expect_tx(&sm.q_full, q_bytes);
+      for (int dc = 0; dc < 4; ++dc)
+        ptx::tma_load_4d(sm.q + dc * kChunkBytes, &tmQ, &sm.q_full, dc * 64, r0, g * p.gqa, b);
+      const int total = 2 * n_tiles;
+      int issued = 0;
+      for (int it = 0; it < total; ++it) {
+        const int slot = it & 1;
+        if (it >= kSlots &&
+            !ptx::mbar_wait(&sm.kv_empty[slot], ((it >> 1) & 1) ^ 1, tmo, &sm.abort)) {
+          fail(sm, p);
+          break;
+        }
+        bool is_v;
+        int j;
+        item_kind(it, n_tiles, is_v, j);
+        ptx::mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
+        const CUtensorMap* tm = is_v ? &tmV : &tmK;
+        for (int dc = 0; dc < 4; ++dc)
+          ptx::tma_load_3d(sm.kv[slot] + dc * kChunkBytes, tm, &sm.kv_full[slot], dc * 64, j * kN,
+                           bg);
+        issued = it + 1;
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      for (int it = max(0, issued - kSlots); it < issued; ++it)
+        ptx::mbar_wait(&sm.kv_full[it & 1], (it >> 1) & 1, tmo, &sm.zero);
+      ptx::mbar_wait(&sm.q_full, 0, tmo, &sm.zero);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = ptx::mbar_wait(&sm.q_full, 0, tmo, &sm.abort);
+      ptx::tc_fence_after();
+      const uint32_t qa = ptx::smem_addr(sm.q);
+      int it = 0;
+      auto issue_s = [&](int j) -> bool {
+        const int slot = it & 1;
+        if (!ptx::mbar_wait(&sm.kv_full[slot], (it >> 1) & 1, tmo, &sm.abort)) return false;
+        ptx::tc_fence_after();
+        const uint32_t ka = ptx::smem_addr(sm.kv[slot]);
+        const uint32_t d = tmem + kTmS + 128u * uint32_t(j & 1);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint32_t off = uint32_t(kk >> 2) * kChunkBytes + uint32_t(kk & 3) * 32u;
+          ptx::mma_ss(d, ptx::sdesc_sw128(qa + off, 16, 1024), ptx::sdesc_sw128(ka + off, 16, 1024),
+                      kIdescS, kk > 0);
+        }
+        ptx::tc_commit(&sm.s_full[j & 1]);
+        ptx::tc_commit(&sm.kv_empty[slot]);
+        ++it;
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        if (!ptx::mbar_wait(&sm.p_full[j & 1], (j >> 1) & 1, tmo, &sm.abort)) return false;
+        const int slot = it & 1;
+        if (!ptx::mbar_wait(&sm.kv_full[slot], (it >> 1) & 1, tmo, &sm.abort)) return false;
+        ptx::tc_fence_after();
+        const uint32_t va = ptx::smem_addr(sm.kv[slot]);
+        const uint32_t pa = tmem + kTmS + 128u * uint32_t(j & 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acol = kk < 4 ? uint32_t(kk) * 8u : 64u + uint32_t(kk - 4) * 8u;
+          ptx::mma_ts(tmem + kTmO, pa + acol, ptx::sdesc_sw128(va + uint32_t(kk) * 2048u, 16384, 1024),
+                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::tc_commit(&sm.pv_done);
+        ptx::tc_commit(&sm.kv_empty[slot]);
+        ++it;
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 1; ok && j < n_tiles; ++j) {
+        ok = issue_s(j);
+        if (ok) ok = issue_pv(j - 1);
+      }
+      if (ok) ok = issue_pv(n_tiles - 1);
+      if (ok) {
+        ptx::tc_commit(&sm.o_final);
+      } else {
+        fail(sm, p);
+      }
+      // Every MMA issued so far must finish before tensor memory is released.
+      ptx::tc_commit(&sm.drain);
+      ptx::mbar_wait(&sm.drain, 0, tmo, &sm.zero);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int sw = warp - 2;
+    const int half = sw >> 2;
+    const int lq = warp & 3;
+    const int row = lq * 32 + lane;
+    const uint32_t bar_id = 1 + lq;
+    const int hh = row / p.R;
+    const int rr = row - hh * p.R;
+    const bool valid = (row < p.R * p.gqa) && (r0 + rr < p.Lq);
+    const int q = r0 + rr;
+    const int lim = valid ? p.kv_offset + q + 1 : p.kv_offset + r0 + 1;
+    const uint32_t trow = tmem + (uint32_t(lq * 32) << 16);
+
+    float m_run = -INFINITY;
+    float l_part = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int buf = j & 1;
+      bool mine = warp_all(ptx::mbar_wait(&sm.s_full[buf], (j >> 1) & 1, tmo, &sm.abort)) &&
+                  !sm.abort;
+      uint32_t s[64];
+      float mx = -INFINITY;
+      if (mine) {
+        ptx::tc_fence_after();
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+        ptx::tmem_ld32_wait(trow + kTmS + 128u * buf + 64u * half, s0);
+        ptx::tmem_ld32_wait(trow + kTmS + 128u * buf + 64u * half + 32u, s1);
+        const int key0 = j * kN + half * 64;
+        if (key0 + 64 > lim) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (key0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        mx *= kScaleLog2;
+      }
+      sm.red[buf][half][row] = mx;
+      sm.ok[buf][half][row] = mine ? 1 : 0;
+      ptx::named_bar_sync(bar_id, 64);
+      ok = mine && sm.ok[buf][half ^ 1][row];
+      if (!ok) break;
+      const float tmax = fmaxf(mx, sm.red[buf][half ^ 1][row]);
+      bool store_ok = true;
+      if (j == 0) {
+        m_run = tmax;
+      } else if (__any_sync(0xffffffffu, tmax > m_run + kRescaleThreshold)) {
+        // Warp-uniform (tcgen05.ld/st are warp-collective); the partner warp holds the
+        // same rows, so it takes the same branch.  Rows whose max did not move keep
+        // alpha = 1.
+        const float m_new = fmaxf(m_run, tmax);
+        const float alpha = ex2(m_run - m_new);
+        m_run = m_new;
+        l_part *= alpha;
+        // O must hold PV_{j-1} before it is rescaled.
+        store_ok = warp_all(ptx::mbar_wait(&sm.pv_done, (j - 1) & 1, tmo, &sm.abort));
+        if (store_ok) {
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            const uint32_t ta = trow + kTmO + 128u * half + 32u * cc;
+            ptx::tmem_ld32_wait(ta, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            ptx::tmem_st32_wait(ta, o);
+          }
+        }
+      }
+      if (!store_ok) {
+        fail(sm, p);
+        continue;  // the next exchange stops both threads of the pair
+      }
+      const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+      float lsum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), kScaleLog2, -msub));
+        const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), kScaleLog2, -msub));
+        lsum += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l_part += lsum;
+      ptx::tmem_st32_wait(trow + kTmS + 128u * buf + 64u * half, pk);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.p_full[buf]);
+    }
+    if (!ok) fail(sm, p);
+
+    // ---------------------------------------------------------------- epilogue
+    bool fin = ok && warp_all(ptx::mbar_wait(&sm.o_final, 0, tmo, &sm.abort));
+    const int pb = n_tiles & 1;   // parity slot not used by the last tile's exchange
+    sm.red[pb][half][row] = l_part;
+    sm.ok[pb][half][row] = fin ? 1 : 0;
+    ptx::named_bar_sync(bar_id, 64);
+    fin = fin && sm.ok[pb][half ^ 1][row];
+    if (fin) {
+      ptx::tc_fence_after();
+      const float l_tot = l_part + sm.red[pb][half ^ 1][row];
+      const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const int h = g * p.gqa + hh;
+      const size_t row_off = (size_t(b) * p.Hq + h) * size_t(p.Lq) + size_t(q);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        ptx::tmem_ld32_wait(trow + kTmO + 128u * half + 32u * cc, o);
+        if (valid) {
+          const int col0 = half * 128 + cc * 32;
+          float gs[32];
+          if (p.G != nullptr) {
+            const uint4* gp = reinterpret_cast<const uint4*>(p.G + row_off * kHeadDim + col0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 u = __ldg(gp + v);
+              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16x2(w[e]);
+                gs[v * 8 + 2 * e] = gate_sigmoid(f.x);
+                gs[v * 8 + 2 * e + 1] = gate_sigmoid(f.y);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) gs[c] = 1.f;
+          }
+          uint4* op = reinterpret_cast<uint4*>(p.out + row_off * kHeadDim + col0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(o[v * 8 + 0]) * inv_l * gs[v * 8 + 0],
+                              __uint_as_float(o[v * 8 + 1]) * inv_l * gs[v * 8 + 1]);
+            u.y = pack_bf16x2(__uint_as_float(o[v * 8 + 2]) * inv_l * gs[v * 8 + 2],
+                              __uint_as_float(o[v * 8 + 3]) * inv_l * gs[v * 8 + 3]);
+            u.z = pack_bf16x2(__uint_as_float(o[v * 8 + 4]) * inv_l * gs[v * 8 + 4],
+                              __uint_as_float(o[v * 8 + 5]) * inv_l * gs[v * 8 + 5]);
+            u.w = pack_bf16x2(__uint_as_float(o[v * 8 + 6]) * inv_l * gs[v * 8 + 6],
+                              __uint_as_float(o[v * 8 + 7]) * inv_l * gs[v * 8 + 7]);
+            op[v] = u;
+          }
+        }
+      }
+      if (valid && half == 0 && p.lse != nullptr)
+        p.lse[row_off] = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
+    } else {
+      fail(sm, p);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool encode_bf16(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank,
+                 const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base),
+                  dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStream_t stream,
+                           bool* encode_failed) {
+  *encode_failed = false;
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) {
+    *encode_failed = true;
+    return cudaErrorNotSupported;
+  }
+  const int gqa = a.Hq / a.Hkv;
+  const int R = prefill_rows_per_tile(gqa);
+  CUtensorMap tq, tk, tv;
+  {
+    const cuuint64_t dims[4] = {256, cuuint64_t(a.Lq), cuuint64_t(a.Hq), cuuint64_t(a.B)};
+    const cuuint64_t str[3] = {512, cuuint64_t(a.Lq) * 512, cuuint64_t(a.Hq) * a.Lq * 512};
+    const cuuint32_t box[4] = {64, cuuint32_t(R), cuuint32_t(gqa), 1};
+    if (!encode_bf16(fn, &tq, a.Q, 4, dims, str, box)) *encode_failed = true;
+  }
+  {
+    // Only keys a row of the call can see are addressable; TMA zero-fills the rest.
+    const cuuint64_t dims[3] = {256, cuuint64_t(a.kv_offset + a.Lq), cuuint64_t(a.B) * a.Hkv};
+    const cuuint64_t str[2] = {512, cuuint64_t(a.Lkv) * 512};
+    const cuuint32_t box[3] = {64, cuuint32_t(kN), 1};
+    if (!encode_bf16(fn, &tk, a.K, 3, dims, str, box)) *encode_failed = true;
+    if (!encode_bf16(fn, &tv, a.V, 3, dims, str, box)) *encode_failed = true;
+  }
+  if (*encode_failed) return cudaErrorInvalidValue;
+
+  Params p;
+  p.G = static_cast<const __nv_bfloat16*>(a.G);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Lq = a.Lq;
+  p.kv_offset = a.kv_offset;
+  p.gqa = gqa;
+  p.R = R;
+  p.n_rtiles = (a.Lq + R - 1) / R;
+  p.ctl = ctl;
+
+  const size_t smem = sizeof(Smem) + 1024;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(smem));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const long long grid = (long long)p.n_rtiles * a.B * a.Hkv;
+  prefill_kernel<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -1,0 +1,174 @@
+/*
+ * gqa_attn.h - C ABI of libgqa_attn.so: causal grouped-query attention at
+ * head_dim 256 with sigmoid output gating, for NVIDIA GB300 (sm_103a).
+ *
+ *     out = softmax(Q K^T / 16 + causal/offset mask) V  (elementwise *)  sigmoid(G)
+ *
+ * Sources for the operation (page, section):
+ *   - TensorFold PR #1009, "Receipt", attention contract paragraph: decode rows and
+ *     prompt rows at 24 query heads over 4 KV heads and 16 over 2, checked against
+ *     float64 gated attention; decode runs over cache chunks whose partial results
+ *     are merged (its control "a merge dropping later tail chunks").
+ *   - TensorFold PR #1009, "Design: one engine": gated full attention layers.
+ *   - d-inference PR #640, "Summary": head_dim 256 attention, FP16 and BF16 symbols.
+ *   - DS4Server issue113 README, opening rule: query heads inside each KV group
+ *     share that group's K/V.
+ *
+ * Conventions shared by every entry point:
+ *   - head_dim D is fixed at 256; every tensor is bf16, contiguous, row-major,
+ *     and 16-byte aligned, unless stated otherwise.
+ *   - Query head h reads KV head h / (Hq / Hkv) (consecutive groups).
+ *   - Scores are scaled by 1/16 = 1/sqrt(256).  Softmax sums and all accumulation
+ *     are fp32; the output is rounded once to bf16 (round to nearest even).
+ *   - G may be NULL: no gate (the output is the plain attention).
+ *   - lse outputs, when requested, are fp32 natural-log sum-exp of the scaled
+ *     scores over the keys a row sees (-inf for a row that sees no key).
+ *   - A row that sees no key outputs zeros.
+ *   - Ownership: the caller owns every buffer.  The library never allocates
+ *     device memory; the decode workspace is caller-provided.
+ *   - Streams: every call is asynchronous on `stream` (may be 0 = legacy default
+ *     stream).  Pointers are device pointers unless a parameter says "host".
+ *   - Errors: arguments are validated on the host before any launch; an invalid
+ *     call returns GQA_ERR_INVALID_ARG (or GQA_ERR_UNSUPPORTED) and launches
+ *     nothing.  A failed launch returns GQA_ERR_CUDA.  Conditions only the device
+ *     can see (a kv length beyond the cache, a wait that timed out) are recorded
+ *     in a device status word that gqa_last_device_status() reads; the kernel
+ *     skips the offending work instead of faulting.
+ *   - A call with no rows (Lq = 0, T = 0, N = 0) returns GQA_OK and launches
+ *     nothing.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (a cudaStream_t). */
+typedef void* gqa_stream_t;
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1, /* bad size, NULL or misaligned pointer, bad geometry   */
+  GQA_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement         */
+  GQA_ERR_CUDA = 3,        /* a CUDA call or launch failed                         */
+  GQA_ERR_TIMEOUT = 4,     /* device: a bounded wait ran out (kernel returned)     */
+  GQA_ERR_WORKSPACE = 5,   /* decode workspace too small                           */
+  GQA_ERR_DEVICE_RANGE = 6 /* device: kv_lens / cu_rows out of range (work skipped) */
+} gqa_status;
+
+/* Static, NUL-terminated description of a status code. */
+const char* gqa_status_string(int status);
+
+/* Library version, "major.minor.patch". */
+const char* gqa_version(void);
+
+/*
+ * Prompt rows (prefill), possibly a chunk of a longer prompt.
+ *
+ *   out[b,h,i,:] = sum_{j <= kv_offset+i} softmax_j(Q[b,h,i,:].K[b,g,j,:]/16) V[b,g,j,:]
+ *                  * sigmoid(G[b,h,i,:]),   g = h / (Hq/Hkv)
+ *
+ * Q, G, out: [B, Hq, Lq, 256] bf16.  K, V: [B, Hkv, Lkv, 256] bf16.
+ * lse_out: NULL, or fp32 [B, Hq, Lq].
+ * Row i sits at absolute position kv_offset + i; keys at positions above
+ * kv_offset + Lq - 1 are never read (they may hold anything, NaN included).
+ * Requires B, Hq, Hkv >= 1, Hq % Hkv == 0, Hq/Hkv <= 128, Lq >= 0,
+ * kv_offset >= 0, kv_offset + Lq <= Lkv, Lkv < 2^31.
+ * Runs on tcgen05 tensor cores (TMEM accumulators, TMA-staged tiles).
+ */
+int gqa_attn_prefill(const void* Q, const void* K, const void* V, const void* G,
+                     void* out, float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv,
+                     int kv_offset, gqa_stream_t stream);
+
+/*
+ * Decode (one row per sequence) and chain verify (r_b rows per sequence, causal
+ * within the rows) against a contiguous KV cache.
+ *
+ * Q, G, out: [T, Hq, 256] bf16, token-major; the rows of sequence b are tokens
+ *   cu_rows[b] .. cu_rows[b+1]-1 (T = cu_rows[B]).
+ * Kcache, Vcache: [B, Hkv, Lcap, 256] bf16.
+ * kv_lens: int32 [B] (device): keys held for sequence b, counting its new rows;
+ *   row i (0-based of r_b) sees keys j < kv_lens[b] - r_b + i + 1.  Cache rows at
+ *   or beyond kv_lens[b] are never read (they may hold anything, NaN included).
+ * cu_rows: int32 [B+1] (device) exclusive prefix sum of rows, or NULL for one row
+ *   per sequence (then T must equal B and max_rows must be 1).
+ * lse_out: NULL, or fp32 [T, Hq].
+ * T, max_rows, max_kv_len (host): total rows, an upper bound on r_b and on
+ *   kv_lens[b]; they size the grid.  Sequences whose kv_lens/cu_rows break these
+ *   bounds (or kv_lens[b] < r_b, or kv_lens[b] > Lcap) are skipped on the device
+ *   and GQA_ERR_DEVICE_RANGE is recorded.
+ * workspace: device buffer of at least gqa_attn_decode_workspace_size() bytes,
+ *   16-byte aligned; holds the split partial results.
+ * The call runs gqa_attn_decode_split() then attn_lse_merge() on `stream`.
+ */
+size_t gqa_attn_decode_workspace_size(int B, int T, int Hq, int Hkv, int max_rows,
+                                      int max_kv_len);
+int gqa_attn_decode(const void* Q, const void* Kcache, const void* Vcache, const void* G,
+                    const int* kv_lens, const int* cu_rows, void* out, float* lse_out,
+                    int B, int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                    void* workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+/*
+ * The split plan gqa_attn_decode uses: the number of key splits S and the keys
+ * per split (a multiple of 64).  Split s of sequence b covers keys
+ * [s*split_keys, min((s+1)*split_keys, kv_lens[b])).  Host-only; returns
+ * GQA_ERR_INVALID_ARG for bad sizes.
+ */
+int gqa_attn_decode_plan(int B, int T, int Hq, int Hkv, int max_rows, int max_kv_len,
+                         int* num_splits, int* split_keys);
+
+/*
+ * First half of gqa_attn_decode: per (sequence, KV group, key split), the
+ * attention of all of the group's query heads x rows over the split's keys,
+ * written as normalised partial results for attn_lse_merge():
+ *   O_parts  fp32 [num_splits, T*Hq, 256]: sum_j p_j V_j / l over the split's keys
+ *   lse_parts fp32 [num_splits, T*Hq]: m + ln l, -inf when the row sees no key of
+ *   the split (its O_parts row is then not written).
+ * Row n of the parts is output row (t, h) with n = t*Hq + h.
+ * num_splits >= 1 and split_keys (a positive multiple of 64) with
+ * num_splits*split_keys >= max_kv_len; gqa_attn_decode_plan() gives the defaults.
+ */
+int gqa_attn_decode_split(const void* Q, const void* Kcache, const void* Vcache,
+                          const int* kv_lens, const int* cu_rows, float* O_parts,
+                          float* lse_parts, int B, int T, int Hq, int Hkv, int Lcap,
+                          int max_rows, int max_kv_len, int num_splits, int split_keys,
+                          gqa_stream_t stream);
+
+/*
+ * Merge S partial results of N rows computed over disjoint key sets:
+ *   out[n,:] = (sum_s exp(lse_s) O_s[n,:]) / (sum_s exp(lse_s))  * sigmoid(G[n,:])
+ * O_parts fp32 [S, N, 256], each part normalised (O_s / l_s); lse_parts fp32
+ * [S, N] = m_s + ln l_s, -inf for an empty part (weight 0, its O row is never
+ * read).  G: NULL (no gate) or bf16 [N, 256].  out: bf16 [N, 256].  lse_out:
+ * NULL or fp32 [N].  A row whose parts are all empty gets zeros and lse -inf.
+ * This is the tail-chunk merge of the TensorFold attention contract; it also lets
+ * a caller compose results over longer contexts or key shards.
+ * O_parts and lse_parts need 16- and 4-byte alignment.
+ */
+int attn_lse_merge(const float* O_parts, const float* lse_parts, int S, int N,
+                   const void* G, void* out, float* lse_out, gqa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word that the
+ * kernels set (GQA_ERR_TIMEOUT, GQA_ERR_DEVICE_RANGE); GQA_OK when clear.
+ * Returns GQA_ERR_CUDA if the synchronisation fails.
+ */
+int gqa_last_device_status(gqa_stream_t stream);
+
+/*
+ * Bound (in nanoseconds) on every spin wait inside the kernels; after it runs
+ * out the kernel records GQA_ERR_TIMEOUT and returns.  Default 2e9 (2 s).
+ * Host-only setter, takes effect for later launches.  Values < 1e6 are clamped
+ * to 1e6.
+ */
+void gqa_set_wait_timeout_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

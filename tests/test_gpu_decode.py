@@ -1,0 +1,178 @@
+"""Decode / chain verify and the LSE merge on the GPU, through the C ABI, against the
+float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_head_gated_gb300 as G
+import oracle
+from synth import inputs as S
+from tests.parity import assert_parity, fails_parity, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def dev(x):
+    return (x.q.to(DEV), x.k_cache.to(DEV), x.v_cache.to(DEV), x.g.to(DEV), x.kv_lens.to(DEV),
+            x.cu_rows.to(DEV))
+
+
+def run(x, gate=True, lse=False, one_row=False):
+    q, kc, vc, g, kv, cu = dev(x)
+    r = G.decode(q, kc, vc, g if gate else None, kv, None if one_row else cu,
+                 max_rows=max(x.rows) if x.rows else 1, max_kv_len=int(x.kv_lens.max()),
+                 return_lse=lse)
+    assert G.last_device_status() == 0
+    return r
+
+
+def ref(x, gate=True):
+    return oracle.decode(to_f64(x.q), to_f64(x.k_cache), to_f64(x.v_cache),
+                         to_f64(x.g) if gate else None, x.kv_lens.tolist(), x.cu_rows.tolist())
+
+
+def test_decode_27b_workload():
+    """16 sequences, one row each, kv lengths 1987..32233 in a 32768-key cache whose
+    padding is NaN; the bench's launch configuration."""
+    x = S.decode_27b()
+    out, lse = run(x, lse=True, one_row=True)
+    r_out, r_lse = ref(x)
+    assert_parity(out, r_out, "decode 27B")
+    np.testing.assert_allclose(to_f64(lse), r_lse, rtol=0, atol=2e-3)
+
+
+def test_verify_35b_workload():
+    """8 sequences with 1..32 verify rows, kv lengths 4271..45513 in a 65536-key cache."""
+    x = S.verify_35b()
+    out, lse = run(x, lse=True)
+    r_out, r_lse = ref(x)
+    assert_parity(out, r_out, "verify 35B")
+    np.testing.assert_allclose(to_f64(lse), r_lse, rtol=0, atol=2e-3)
+
+
+SWEEP = [
+    # Hq, Hkv, rows, kv_lens
+    (4, 4, [1, 1, 1], [1, 2, 3]),
+    (8, 2, [1, 1, 1, 1], [127, 128, 129, 63]),
+    (24, 4, [1, 1], [8190, 8191]),
+    (24, 4, [1, 1], [8192, 8193]),
+    (16, 2, [3, 4, 8], [3, 100, 4097]),
+    (16, 2, [16, 32], [40, 1000]),
+    (12, 1, [5, 2], [700, 5]),                # GQA 12: 60 packed rows
+    (32, 4, [32, 7], [300, 3000]),            # GQA 8 x 32 rows = 256 packed rows
+    (6, 6, [64], [2000]),                     # 64 rows, GQA 1
+    (16, 1, [9, 0, 1], [500, 0, 33]),         # a sequence with no rows
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,rows,kv", SWEEP)
+def test_decode_sweep(Hq, Hkv, rows, kv):
+    x = S.make_decode(len(rows), Hq, Hkv, rows, kv, Lcap=max(kv) + 7, seed=sum(kv) + Hq)
+    out, lse = run(x, lse=True)
+    r_out, r_lse = ref(x)
+    assert_parity(out, r_out, f"decode {Hq,Hkv,rows,kv}")
+    np.testing.assert_allclose(to_f64(lse), r_lse, rtol=0, atol=2e-3)
+
+
+def test_decode_ungated():
+    x = S.make_decode(3, 8, 2, [1, 2, 3], [10, 200, 3000], seed=12)
+    assert_parity(run(x, gate=False), ref(x, gate=False)[0], "ungated")
+
+
+def test_padding_and_future_keys_bit_exact():
+    """Cache padding (NaN vs other garbage) never changes an output; perturbing the
+    keys of later verify rows leaves earlier rows bit for bit unchanged."""
+    x = S.make_decode(2, 16, 2, [4, 8], [900, 5000], Lcap=5100, seed=13)
+    a = run(x)
+    x.k_cache[0, :, 900:] = 7.0
+    x.v_cache[1, :, 5000:] = float("-inf")
+    b = run(x)
+    assert torch.equal(a, b)
+    # sequence 1 rows: kv_len 5000, 8 rows at positions 4992..4999; perturb 4996..4999
+    x.k_cache[1, :, 4996:5000] = (x.k_cache[1, :, 4996:5000].float() * 3).to(torch.bfloat16)
+    x.v_cache[1, :, 4996:5000] = (x.v_cache[1, :, 4996:5000].float() - 2).to(torch.bfloat16)
+    c = run(x)
+    t0 = 4
+    assert torch.equal(a[:t0 + 4], c[:t0 + 4])
+    assert not torch.equal(a[t0 + 4:], c[t0 + 4:])
+
+
+def test_verify_row_equals_decode_row():
+    """Row i of an r-row verify equals a one-row decode at kv_len - r + i + 1."""
+    r, L = 8, 3000
+    x = S.make_decode(1, 16, 2, [r], [L], seed=14)
+    full = run(x)
+    for i in [0, 3, 7]:
+        y = S.DecodeInputs(x.q[i:i + 1].clone(), x.k_cache, x.v_cache, x.g[i:i + 1].clone(),
+                           torch.tensor([L - r + i + 1], dtype=torch.int32),
+                           torch.tensor([0, 1], dtype=torch.int32), 0)
+        one = run(y, one_row=True)
+        assert (one.float() - full[i:i + 1].float()).abs().max().item() <= 4e-3
+
+
+def test_split_then_merge_equals_decode():
+    x = S.make_decode(4, 24, 4, [1, 2, 1, 3], [5000, 70, 12000, 900], seed=15)
+    out = run(x)
+    q, kc, vc, g, kv, cu = dev(x)
+    op, lp = G.decode_split(q, kc, vc, kv, cu, max_rows=3, max_kv_len=12000)
+    merged = G.lse_merge(op, lp, g)
+    assert torch.equal(merged.view_as(out), out)
+    # any split count gives the same result within tolerance
+    op2, lp2 = G.decode_split(q, kc, vc, kv, cu, max_rows=3, max_kv_len=12000, num_splits=1,
+                              split_keys=12032)
+    merged2 = G.lse_merge(op2, lp2, g)
+    assert (merged2.float() - merged.float()).abs().max().item() <= 4e-3
+    assert G.last_device_status() == 0
+
+
+def test_merge_against_oracle():
+    """Random normalised parts, some empty (lse -inf, O full of NaN that must not be
+    read)."""
+    gen = torch.Generator().manual_seed(16)
+    Sn, N = 7, 300
+    o = torch.randn(Sn, N, 256, generator=gen)
+    l = torch.randn(Sn, N, generator=gen) * 3
+    empty = torch.rand(Sn, N, generator=gen) < 0.3
+    l[empty] = float("-inf")
+    o[empty] = float("nan")
+    l[:, 5] = float("-inf")                          # a row with no key at all
+    gate = (torch.randn(N, 256, generator=gen) * 2).to(torch.bfloat16)
+    out, lse = G.lse_merge(o.to(DEV), l.to(DEV), gate.to(DEV), return_lse=True)
+    r_out, r_lse = oracle.lse_merge(o.double().numpy(), l.double().numpy(), to_f64(gate))
+    assert_parity(out, r_out, "merge")
+    assert torch.all(out[5] == 0) and lse[5].item() == float("-inf")
+    fin = np.isfinite(r_lse)
+    np.testing.assert_allclose(to_f64(lse)[fin], r_lse[fin], rtol=0, atol=1e-5)
+
+
+def test_merge_dropping_a_chunk_control():
+    """Control: a merge that drops the last part must fail parity."""
+    gen = torch.Generator().manual_seed(17)
+    o = torch.randn(4, 64, 256, generator=gen)
+    l = torch.randn(4, 64, generator=gen)
+    out = G.lse_merge(o.to(DEV), l.to(DEV))
+    bad, _ = oracle.lse_merge(o[:3].double().numpy(), l[:3].double().numpy())
+    assert fails_parity(out, bad)
+
+
+def test_empty_decode_is_noop():
+    q = torch.empty(0, 8, 256, dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros(2, 2, 8, 256, dtype=torch.bfloat16, device=DEV)
+    kv = torch.tensor([0, 0], dtype=torch.int32, device=DEV)
+    cu = torch.tensor([0, 0, 0], dtype=torch.int32, device=DEV)
+    out = G.decode(q, kc, kc, q, kv, cu, max_rows=1, max_kv_len=1)
+    assert out.shape == (0, 8, 256)
+
+
+def test_device_range_error_is_recorded():
+    """A kv length beyond the cache is caught on the device: the sequence is skipped
+    and the status word says so; the context stays usable."""
+    x = S.make_decode(2, 8, 2, [1, 1], [10, 20], Lcap=32, seed=18)
+    q, kc, vc, g, kv, cu = dev(x)
+    kv_bad = torch.tensor([10, 40], dtype=torch.int32, device=DEV)
+    G.decode(q, kc, vc, g, kv_bad, None, max_rows=1, max_kv_len=32)
+    assert G.last_device_status() == 6
+    assert G.last_device_status() == 0
+    out = G.decode(q, kc, vc, g, kv, None, max_rows=1, max_kv_len=20)
+    assert_parity(out, ref(x)[0], "after range error")
