@@ -75,63 +75,113 @@ def prefill_flops(x):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons of one GPU while the
+    timed region runs.  Reads NVML (libnvidia-ml, read-only queries) from a thread
+    every ~2 ms, so even a few-millisecond region gets samples; falls back to an
+    `nvidia-smi -lms` subprocess when NVML cannot be loaded."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index):
+    def __init__(self, device_index, period_s=0.002):
         self.dev = device_index
-        self.proc = None
-        self.lines = []
+        self.period = period_s
+        self.samples = []          # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
         self._t = None
+        self._nvml = None
+        self._h = None
+        self._proc = None
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        # The NVML index of the CUDA device: match by PCI bus id.
+        # The NVML handle of the CUDA device: by UUID (robust to CUDA_VISIBLE_DEVICES),
+        # else by index.
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.dev)
+        uuid = getattr(props, "uuid", None)
+        ok = False
+        if uuid is not None:
+            u = str(uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            ok = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.dev, ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self._nvml, self._h = lib, h
+        self._reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def _poll(self):
+        import ctypes
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if self._reason_fn(self._h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), int(r)))
+            time.sleep(self.period)
+
+    def _smi(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown")
+        self._proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "20",
+                                       "-i", str(self.dev)],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        bits = [0x4, 0x8, 0x20, 0x40]
+        for line in self._proc.stdout:
+            f = [c.strip() for c in line.split(",")]
+            try:
+                self.max_mhz = float(f[1])
+                r = sum(b for b, v in zip(bits, f[2:6]) if v.lower().startswith("active"))
+                self.samples.append((float(f[0]), r))
+            except (ValueError, IndexError):
+                pass
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.dev)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
-            self._t.start()
-        except (OSError, ValueError):
-            self.proc = None
+            self._nvml_open()
+            self.source = "nvml"
+            self._t = threading.Thread(target=self._poll, daemon=True)
+        except (OSError, AttributeError):
+            self.source = "nvidia-smi"
+            self._t = threading.Thread(target=self._smi, daemon=True)
+        self._t.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5.0:   # sampler is live before timing
+            time.sleep(0.001)
+        self.samples.clear()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-            if self._t is not None:
-                self._t.join(timeout=2)
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+        if self._t is not None:
+            self._t.join(timeout=5)
+        if self._nvml is not None:
+            self._nvml.nvmlShutdown()
 
     def summary(self):
-        sms, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [c.strip() for c in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sms.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sms:
+        if not self.samples:
             return None
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sms)}
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if mask & b),
+                "samples": len(self.samples), "source": self.source}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -290,14 +340,15 @@ def bench_prefill(x, steps, warmup, dev):
         G.prefill(q, k, v, g, kv_offset=x.kv_offset, out=out)
     torch.cuda.synchronize()
     pairs = []
-    for _ in range(steps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        G.prefill(q, k, v, g, kv_offset=x.kv_offset, out=out)
-        b.record()
-        pairs.append((a, b))
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for _ in range(steps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            G.prefill(q, k, v, g, kv_offset=x.kv_offset, out=out)
+            b.record()
+            pairs.append((a, b))
+        torch.cuda.synchronize()
     status = G.last_device_status()
     ms = elapsed_ms(pairs)
     # e2e: host buffers in, out back
@@ -318,7 +369,7 @@ def bench_prefill(x, steps, warmup, dev):
         b.synchronize()
         e2e.append(a.elapsed_time(b))
     h2d = sum(t.numel() * 2 for t in (hq, hk, hv, hg))
-    return ms, status, e2e, h2d, hout.numel() * 2
+    return ms, status, e2e, h2d, hout.numel() * 2, clk.summary()
 
 
 def ours(args):
@@ -362,7 +413,8 @@ def ours(args):
     pf = S.prefill_27b()
     flops = prefill_flops(pf)
     pf_steps = max(3, min(args.steps, 10))
-    pf_ms, pf_status, pf_e2e, pf_h2d, pf_d2h = bench_prefill(pf, pf_steps, max(3, args.warmup), dev)
+    pf_ms, pf_status, pf_e2e, pf_h2d, pf_d2h, pf_clk = bench_prefill(pf, pf_steps,
+                                                                     max(3, args.warmup), dev)
     pf_avg = sum(pf_ms) / len(pf_ms)
     pf_tflops = flops / (pf_avg / 1e3) / 1e12
     bf16_peak = float(peaks["bf16_tflops"])
@@ -434,6 +486,7 @@ def ours(args):
                 "e2e": {"value": round(flops / (pf_e2e_avg / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                         "h2d_bytes_per_step": pf_h2d, "d2h_bytes_per_step": pf_d2h},
                 "device_status": pf_status,
+                "clocks": pf_clk,
             },
             "clocks": clk.summary(),
             "device_status": status,

@@ -139,6 +139,7 @@ int gqa_attn_prefill(const void* Q, const void* K, const void* V, const void* G,
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq < 0 || Lkv < 1 || kv_offset < 0 ||
       (long long)kv_offset + Lq > Lkv)
     return GQA_ERR_INVALID_ARG;
+  if (Lq == 0) return GQA_OK;   // nothing to do (an empty tensor may have a null pointer)
   if (Q == nullptr || K == nullptr || V == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 16) ||
       (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)))
@@ -146,7 +147,6 @@ int gqa_attn_prefill(const void* Q, const void* K, const void* V, const void* G,
   if (Hq / Hkv > 128) return GQA_ERR_UNSUPPORTED;
   if ((long long)Hq * Lq >= (1LL << 31) || (long long)B * Hkv >= (1LL << 31))
     return GQA_ERR_UNSUPPORTED;
-  if (Lq == 0) return GQA_OK;
   const long long grid = (long long)ceil_div(Lq, prefill_rows_per_tile(Hq / Hkv)) * B * Hkv;
   if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
   LaunchCtl ctl;
@@ -182,13 +182,13 @@ int gqa_attn_decode_split(const void* Q, const void* Kcache, const void* Vcache,
   if (num_splits < 1 || split_keys < 64 || split_keys % 64 != 0 ||
       (long long)num_splits * split_keys < max_kv_len)
     return GQA_ERR_INVALID_ARG;
+  if (T == 0) return GQA_OK;
   if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
       O_parts == nullptr || lse_parts == nullptr)
     return GQA_ERR_INVALID_ARG;
   if (!aligned(Q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(O_parts, 16) ||
       !aligned(lse_parts, 4) || !aligned(kv_lens, 4) || (cu_rows && !aligned(cu_rows, 4)))
     return GQA_ERR_INVALID_ARG;
-  if (T == 0) return GQA_OK;
   const int gqa = Hq / Hkv;
   const long long packed = (long long)max_rows * gqa;
   const int MB = decode_rows_per_cta(int(packed > (1 << 30) ? (1 << 30) : packed));
@@ -221,13 +221,13 @@ int gqa_attn_decode(const void* Q, const void* Kcache, const void* Vcache, const
                     void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
   const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
   if (st != GQA_OK) return st;
+  if (T == 0) return GQA_OK;
   if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
       out == nullptr)
     return GQA_ERR_INVALID_ARG;
   if (!aligned(out, 16) || (G != nullptr && !aligned(G, 16)) ||
       (lse_out != nullptr && !aligned(lse_out, 4)))
     return GQA_ERR_INVALID_ARG;
-  if (T == 0) return GQA_OK;
   int S = 0, C = 0;
   plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
   const size_t need = workspace_bytes_for(T, Hq, S);

@@ -293,12 +293,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (j == 0) {
         m_run = tmax;
       } else if (__any_sync(0xffffffffu, tmax > m_run + kRescaleThreshold)) {
-        // Warp-uniform (tcgen05.ld/st are warp-collective); the partner warp holds the
-        // same rows, so it takes the same branch.  Rows whose max did not move keep
-        // alpha = 1.
-        const float m_new = fmaxf(m_run, tmax);
-        const float alpha = ex2(m_run - m_new);
-        m_run = m_new;
+        // The branch is warp-uniform (tcgen05.ld/st are warp-collective; the partner warp
+        // holds the same rows, so it takes it too), but only rows whose own max rose past
+        // the threshold move it; the others multiply by exactly 1, so every row's result
+        // depends on its own scores alone.
+        const bool need = tmax > m_run + kRescaleThreshold;
+        const float alpha = need ? ex2(m_run - tmax) : 1.f;
+        if (need) m_run = tmax;
         l_part *= alpha;
         // O must hold PV_{j-1} before it is rescaled.
         store_ok = warp_all(ptx::mbar_wait(&sm.pv_done, (j - 1) & 1, tmo, &sm.abort));

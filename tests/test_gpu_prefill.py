@@ -108,7 +108,7 @@ def test_chunked_equals_whole():
 def test_one_key_too_far_control():
     """Control: the oracle with one extra visible key per row must fail parity against
     the GPU output (the checker can see a masking error)."""
-    x = S.make_prefill(1, 8, 2, 64, seed=10)
+    x = S.make_prefill(1, 8, 2, 64, Lkv=72, seed=10)    # a spare key past the prompt
     out = run(x)
     orig = oracle.attention.prefill_visible
     try:
