@@ -108,6 +108,18 @@ int run_split(const void* Q, const void* Kc, const void* Vc, const int* kv_lens,
 }
 
 }  // namespace
+
+int decode_check_args(int B, int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                      bool has_cu_rows) {
+  return check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, has_cu_rows);
+}
+void decode_plan_current_device(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int* S,
+                                int* C) {
+  plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), S, C);
+}
+size_t decode_workspace_bytes(int T, int Hq, int S) { return workspace_bytes_for(T, Hq, S); }
+bool make_launch_ctl(LaunchCtl* ctl) { return make_ctl(ctl); }
+
 }  // namespace gqa
 
 using namespace gqa;

@@ -55,4 +55,12 @@ struct MergeArgs {
 
 cudaError_t launch_lse_merge(const MergeArgs& a, const LaunchCtl& ctl, cudaStream_t stream);
 
+// Host-side pieces of gqa_attn_decode shared with the no-allocation entry point.
+int decode_check_args(int B, int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                      bool has_cu_rows);
+void decode_plan_current_device(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int* S,
+                                int* C);
+size_t decode_workspace_bytes(int T, int Hq, int S);
+bool make_launch_ctl(LaunchCtl* ctl);
+
 }  // namespace gqa

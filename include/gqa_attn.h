@@ -153,6 +153,30 @@ int attn_lse_merge(const float* O_parts, const float* lse_parts, int S, int N,
                    const void* G, void* out, float* lse_out, gqa_stream_t stream);
 
 /*
+ * Decode / chain verify for callers that cannot allocate device memory: serving
+ * loops that must not touch a device allocator between steps (an allocation can
+ * stall on device-wide synchronisation or fail under memory pressure mid-request),
+ * plug-ins whose host application hands them only fixed input and output buffers.
+ * The paper has
+ * no counterpart: this is a library convenience.  Same inputs, outputs, rules and
+ * results as gqa_attn_decode, but the split partial results live in a fixed
+ * 16 MiB area of device memory owned by the library (a file-scope __device__ array,
+ * held by every GPU that loads the library until the process exits), so the caller
+ * passes no workspace; the call itself allocates nothing.
+ * Limit: gqa_attn_decode_workspace_size() for the same sizes must not exceed
+ * 16 MiB (16,777,216 bytes); larger calls return GQA_ERR_WORKSPACE and launch
+ * nothing.
+ * The first call on a device looks up the area's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls on a device share the area: calls whose kernels
+ * may overlap on the GPU (unordered streams) race on it and must not be issued.
+ */
+int gqa_attn_decode_noalloc(const void* Q, const void* Kcache, const void* Vcache,
+                            const void* G, const int* kv_lens, const int* cu_rows, void* out,
+                            float* lse_out, int B, int T, int Hq, int Hkv, int Lcap,
+                            int max_rows, int max_kv_len, gqa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that the
  * kernels set (GQA_ERR_TIMEOUT, GQA_ERR_DEVICE_RANGE); GQA_OK when clear.
  * Returns GQA_ERR_CUDA if the synchronisation fails.
