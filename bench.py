@@ -540,6 +540,40 @@ def reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- ncu cases
+CASES = {
+    # 24/4 heads, 4096 causal rows: 160 MB of Q/K/V/G/out (> L2), ~0.2 ms per launch
+    "prefill_4k": lambda: S.make_prefill(1, 24, 4, 4096, seed=2, outlier_frac=0.01),
+    # 16 sequences x 24/4 heads, kv lengths 2048..8192 in a [16,4,8192,256] cache (537 MB)
+    "decode_8k": lambda: S.make_decode(16, 24, 4, [1] * 16,
+                                       [2048 + (b * 389) % 6145 for b in range(16)],
+                                       Lcap=8192, seed=1),
+}
+
+
+def run_case(name, launches, warmup):
+    """Launches one small case `warmup + launches` times and prints nothing to stdout
+    (for profiler captures: select the kernel with -k and skip the warm-up launches)."""
+    import gqa_head_gated_gb300 as G
+    dev = torch.device("cuda", 0)
+    x = CASES[name]()
+    if name.startswith("prefill"):
+        q, k, v, g = (t.to(dev) for t in (x.q, x.k, x.v, x.g))
+        out = torch.empty_like(q)
+        for _ in range(warmup + launches):
+            G.prefill(q, k, v, g, kv_offset=x.kv_offset, out=out)
+    else:
+        q, kc, vc, g = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.g))
+        kv = x.kv_lens.to(dev)
+        for _ in range(warmup + launches):
+            G.decode(q, kc, vc, g, kv, None, max_rows=1, max_kv_len=int(x.kv_lens.max()))
+    torch.cuda.synchronize()
+    st = G.last_device_status()
+    log(f"case {name}: {warmup + launches} launches, device status {st}")
+    if st != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -553,7 +587,12 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per split launch from an ncu capture of this kernel")
     ap.add_argument("--prefill-traffic", type=float, default=None)
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
+                    help="only launch this small case (for ncu captures); no JSON line")
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case, args.steps, args.warmup)
+        return
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
     if args.impl == "reference":
         reference(args)
