@@ -59,8 +59,10 @@ bool make_ctl(LaunchCtl* ctl) {
 
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
-// Decode split plan: aim for about four CTAs per SM over the (sequence, group,
-// row block) units, with splits of whole 64-key steps.
+// Decode split plan: aim for about three waves of resident CTAs over the
+// (sequence, group, row block) units (two CTAs fit per SM up to 32 packed rows, one
+// above), so that ragged kv lengths still leave enough CTAs to balance the SMs;
+// splits are whole 64-key steps.
 int plan_decode(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int num_sms, int* S,
                 int* C) {
   const int gqa = Hq / Hkv;
@@ -68,7 +70,7 @@ int plan_decode(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int num_sm
   const int MB = decode_rows_per_cta(int(packed > (1 << 30) ? (1 << 30) : packed));
   const long long n_rb = (packed + MB - 1) / MB;
   const long long units = (long long)B * Hkv * n_rb;
-  const long long want = 4LL * num_sms;
+  const long long want = (MB <= 32 ? 6LL : 4LL) * num_sms;
   long long s = (want + units - 1) / units;
   const long long steps = (max_kv_len + 63) / 64;
   if (s > steps) s = steps;

@@ -9,8 +9,9 @@
 // p = row * GQA + head), so every K/V byte is read once per split for the whole
 // group (DS4Server issue113 README, opening rule).
 //
-// Memory-bound: K/V tiles of 32 keys (32 KB for K+V) stream through a 4-stage
-// cp.async ring with 16-byte vector copies, coalesced along the 512-byte rows;
+// Memory-bound: K/V tiles of 32 keys (32 KB for K+V) stream through a 3-stage
+// cp.async ring (two CTAs per SM for up to 32 packed rows) with 16-byte vector
+// copies, coalesced along the 512-byte rows;
 // rows at or past the split's end are zero-filled by the copy itself, so cache
 // padding is never read.  Scores and P.V run on bf16 mma.sync (m16n8k16,
 // fp32 accumulate); the online softmax is fp32 with quad-shuffle row reductions.
@@ -23,7 +24,7 @@ namespace gqa {
 namespace {
 
 constexpr int kTK = 32;          // keys per tile
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kThreads = 128;
 constexpr int kRowBytes = 512;   // 256 bf16
 constexpr int kTileBytes = kTK * kRowBytes;   // one of K or V
@@ -215,10 +216,15 @@ decode_split_kernel(const Params p) {
     const uint32_t vb = kb + kTileBytes;
     const uint32_t qb = saddr(sQ);
 
-    // S = Q K^T over this warp's NK keys.
+    // S = Q K^T over this warp's NK keys.  With two n-tiles the 16-step k chain is
+    // split over even and odd steps into independent accumulators (shorter latency).
+    constexpr int KC = NT == 2 ? 2 : 1;
     float sc[NT][4];
+    float sc2[KC][NT][4];
 #pragma unroll
-    for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+    for (int c = 0; c < KC; ++c)
+#pragma unroll
+      for (int i = 0; i < NT; ++i) sc2[c][i][0] = sc2[c][i][1] = sc2[c][i][2] = sc2[c][i][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
       uint32_t a0, a1, a2, a3;
@@ -233,10 +239,19 @@ decode_split_kernel(const Params p) {
         const int r = wk * NK + np * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int ch = 2 * kk + ((lane >> 3) & 1);
         ldsm_x4(kb + swz(r, ch), b0, b1, b2, b3);
-        mma_bf16(sc[2 * np], a0, a1, a2, a3, b0, b1);
-        mma_bf16(sc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        mma_bf16(sc2[kk % KC][2 * np], a0, a1, a2, a3, b0, b1);
+        mma_bf16(sc2[kk % KC][2 * np + 1], a0, a1, a2, a3, b2, b3);
       }
     }
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = sc2[0][i][e];
+#pragma unroll
+        for (int c = 1; c < KC; ++c) v += sc2[c][i][e];
+        sc[i][e] = v;
+      }
     // Mask, online softmax (two rows per thread: g4 and g4 + 8).
     const int key_w = k_lo + tile * kTK + wk * NK;
 #pragma unroll

@@ -28,6 +28,7 @@ lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ ls
   if (n >= N) return;
   const size_t stride = size_t(N);
 
+  // Max over parts, 32 parts per round (lane s reads part s of the round).
   float M = -INFINITY;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse_parts + size_t(s) * stride + n));
 #pragma unroll
@@ -37,22 +38,41 @@ lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ ls
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float ls = __ldg(lse_parts + size_t(s) * stride + n);
-      if (ls == -INFINITY) continue;
-      const float w = __expf(ls - M);
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(O_parts + (size_t(s) * stride + n) * 256 + c0);
-      const float4 a = __ldg(src);
-      const float4 b = __ldg(src + 1);
-      acc[0] += w * a.x;
-      acc[1] += w * a.y;
-      acc[2] += w * a.z;
-      acc[3] += w * a.w;
-      acc[4] += w * b.x;
-      acc[5] += w * b.y;
-      acc[6] += w * b.z;
-      acc[7] += w * b.w;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      // lane s holds the weight of part s0 + s (0 for an empty or missing part)
+      const int sl = s0 + lane;
+      const float ls = sl < S ? __ldg(lse_parts + size_t(sl) * stride + n) : -INFINITY;
+      const float wl = ls == -INFINITY ? 0.f : __expf(ls - M);
+      const int cnt = min(32, S - s0);
+      // Batches of 4 parts: the loads of a batch are issued together.
+      for (int b = 0; b < cnt; b += 4) {
+        float w[4];
+        float4 va[4], vb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          w[u] = __shfl_sync(0xffffffffu, wl, min(b + u, 31));
+          if (b + u >= cnt) w[u] = 0.f;
+          va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (w[u] != 0.f) {
+            const float4* src = reinterpret_cast<const float4*>(
+                O_parts + (size_t(s0 + b + u) * stride + n) * 256 + c0);
+            va[u] = __ldg(src);
+            vb[u] = __ldg(src + 1);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          wsum += w[u];
+          acc[0] += w[u] * va[u].x;
+          acc[1] += w[u] * va[u].y;
+          acc[2] += w[u] * va[u].z;
+          acc[3] += w[u] * va[u].w;
+          acc[4] += w[u] * vb[u].x;
+          acc[5] += w[u] * vb[u].y;
+          acc[6] += w[u] * vb[u].z;
+          acc[7] += w[u] * vb[u].w;
+        }
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;

@@ -7,23 +7,26 @@
 // group share its K/V).  Rows past R*GQA are padding and are never stored.
 //
 // Roles (320 threads):
-//   warp 0      TMA producer: Q tile once, then K_0, K_1, V_0, K_2, V_1, ... into a
-//               2-slot ring of 64 KB tiles (128 keys x 256 dims, 128-byte swizzle).
+//   warp 0      TMA producer: Q tile once, then K_0, K_1, V_0, K_2, V_1, ... as whole
+//               tiles of kN keys x 256 dims (four 128-byte-swizzled column blocks of
+//               64 dims), K tiles into a ring of kKS slots and V tiles into a ring of
+//               kVS slots: K_{j+1} then waits only on S_{j+1-kKS}, never on a PV.
 //   warp 1      TMEM allocator and MMA issuer (one thread):
-//                 S_j = Q K_j^T          M=128, N=128, K=256, A and B from smem
-//                 O  += P_j V_j          M=128, N=256, K=128, A (P) from TMEM
+//                 S_j = Q K_j^T          M=128, N=kN, K=256, A and B from smem
+//                 O  += P_j V_j          M=128, N=256, K=kN, A (P) from TMEM
 //               in the order S_0, S_1, PV_0, S_2, PV_1, ..., so the tensor pipe
 //               works on S_{j+1} while the softmax runs on S_j.
 //   warps 2..9  softmax and epilogue; TMEM lane = tile row, so a thread owns a row
-//               and a pair of warps (w, w+4) shares its lanes: the first takes keys
-//               0..63 of the tile, the second 64..127; the two exchange row maxima
-//               and sums through shared memory.
-// TMEM (512 columns): O at 0..255 (fp32), S double buffer at 256..383 / 384..511;
-// P_j is written as bf16 pairs over the first 32 columns of each half of S_j.
+//               and a pair of warps (w, w+4) shares its lanes: the first takes the
+//               first kN/2 keys of the tile, the second the rest; the two exchange
+//               row maxima and sums through shared memory.
+// TMEM (512 columns): O at 0..255 (fp32), S double buffer at 256 and 256 + kN;
+// P_j is written as bf16 pairs over the first kN/4 columns of each half of S_j.
 //
-// Softmax: fp32, base 2 with the 1/16 scale folded in; the running max is only
-// moved (and O rescaled) when a tile raises it by more than 8 (a factor 256),
-// so p <= 256 and fp32 sums stay exact enough.  Masked keys get probability
+// Softmax: fp32, base 2 with the 1/16 scale folded in; a row's running max (and
+// its O row in TMEM) is only moved when a tile raises it by more than 32, so
+// p <= 2^32 and the fp32 sums stay far from overflow (l < 2^32 x keys) while
+// rescales - a TMEM round trip of the whole O row - stay rare.  Masked keys get probability
 // exactly 0 by selection, never exp(-inf)*0 arithmetic; K/V rows past the last
 // row's horizon are zero-filled by TMA, so nothing outside the visible range is
 // ever multiplied.  Epilogue: out = O / l * sigmoid(G), rounded once to bf16.
@@ -40,22 +43,37 @@ namespace gqa {
 namespace {
 
 constexpr int kM = 128;                       // packed rows per tile
-constexpr int kN = 128;                       // keys per K/V tile
-constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle column)
-constexpr int kTileBytes = 4 * kChunkBytes;   // 128 rows x 256 bf16
-constexpr int kSlots = 2;
+#ifndef GQA_PF_KN
+#define GQA_PF_KN 128
+#endif
+#ifndef GQA_PF_KS
+#define GQA_PF_KS 1
+#endif
+#ifndef GQA_PF_VS
+#define GQA_PF_VS 1
+#endif
+constexpr int kN = GQA_PF_KN;                 // keys per K/V tile (64 or 128)
+constexpr int kKS = GQA_PF_KS;                // K ring slots (whole tiles)
+constexpr int kVS = GQA_PF_VS;                // V ring slots
+constexpr int kSlots = kKS + kVS;
+constexpr int kQChunk = 128 * 128;            // Q: 128 rows x 64 bf16 per column block
+constexpr int kQBytes = 4 * kQChunk;
+constexpr int kChunkBytes = kN * 128;         // K/V: kN rows x 64 bf16 per column block
+constexpr int kTileBytes = 4 * kChunkBytes;   // kN keys x 256 bf16
+constexpr int kHalf = kN / 2;                 // keys per softmax thread per tile
+static_assert(kN == 64 || kN == 128, "key tile of 64 or 128");
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmO = 0;
-constexpr uint32_t kTmS = 256;                // S buffer b at kTmS + 128*b
-constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr uint32_t kTmS = 256;                // S buffer b at kTmS + kN*b
+constexpr float kRescaleThreshold = 32.0f;    // log2 units
 
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kM, kN, 0, 0);    // Q, K both K-major
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kM, 256, 0, 1);  // V is MN-major
 
 struct __align__(1024) Smem {
-  uint8_t q[kTileBytes];
-  uint8_t kv[kSlots][kTileBytes];
+  uint8_t q[kQBytes];
+  uint8_t kv[kSlots][kTileBytes];   // K ring: slots 0..kKS-1, V ring: the rest
   uint64_t q_full;
   uint64_t kv_full[kSlots];
   uint64_t kv_empty[kSlots];
@@ -86,6 +104,23 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+// Position in a ring of tile slots [base, base + n): slot, phase bit, tiles so far.
+struct Ring {
+  int slot;
+  uint32_t phase;
+  int count;
+  int n;
+  int base;
+  __device__ __forceinline__ int at() const { return base + slot; }
+  __device__ __forceinline__ void advance() {
+    ++count;
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 __device__ __forceinline__ void fail(Smem& sm, const Params& p) {
   sm.abort = 1;
@@ -160,29 +195,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const uint32_t q_bytes = 4u * 128u * uint32_t(p.R * p.gqa);
       ptx::mbar_arrive_expect_tx(&sm.q_full, q_bytes);
       for (int dc = 0; dc < 4; ++dc)
-        ptx::tma_load_4d(sm.q + dc * kChunkBytes, &tmQ, &sm.q_full, dc * 64, r0, g * p.gqa, b);
+        ptx::tma_load_4d(sm.q + dc * kQChunk, &tmQ, &sm.q_full, dc * 64, r0, g * p.gqa, b);
       const int total = 2 * n_tiles;
-      int issued = 0;
+      Ring rk{0, 0u, 0, kKS, 0};
+      Ring rv{0, 0u, 0, kVS, kKS};
       for (int it = 0; it < total; ++it) {
-        const int slot = it & 1;
-        if (it >= kSlots &&
-            !ptx::mbar_wait(&sm.kv_empty[slot], ((it >> 1) & 1) ^ 1, tmo, &sm.abort)) {
-          fail(sm, p);
-          break;
-        }
         bool is_v;
         int j;
         item_kind(it, n_tiles, is_v, j);
+        Ring& r = is_v ? rv : rk;
+        const int slot = r.at();
+        if (r.count >= r.n &&
+            !ptx::mbar_wait(&sm.kv_empty[slot], r.phase ^ 1u, tmo, &sm.abort)) {
+          fail(sm, p);
+          break;
+        }
         ptx::mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
         const CUtensorMap* tm = is_v ? &tmV : &tmK;
         for (int dc = 0; dc < 4; ++dc)
           ptx::tma_load_3d(sm.kv[slot] + dc * kChunkBytes, tm, &sm.kv_full[slot], dc * 64, j * kN,
                            bg);
-        issued = it + 1;
+        r.advance();
       }
       // Let every copy this thread started land before the CTA can exit.
-      for (int it = max(0, issued - kSlots); it < issued; ++it)
-        ptx::mbar_wait(&sm.kv_full[it & 1], (it >> 1) & 1, tmo, &sm.zero);
+      for (Ring* r : {&rk, &rv})
+        for (int c = max(0, r->count - r->n); c < r->count; ++c)
+          ptx::mbar_wait(&sm.kv_full[r->base + c % r->n], uint32_t(c / r->n) & 1u, tmo, &sm.zero);
       ptx::mbar_wait(&sm.q_full, 0, tmo, &sm.zero);
     }
     __syncwarp();
@@ -192,40 +230,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       bool ok = ptx::mbar_wait(&sm.q_full, 0, tmo, &sm.abort);
       ptx::tc_fence_after();
       const uint32_t qa = ptx::smem_addr(sm.q);
-      int it = 0;
+      Ring rk{0, 0u, 0, kKS, 0};
+      Ring rv{0, 0u, 0, kVS, kKS};
       auto issue_s = [&](int j) -> bool {
-        const int slot = it & 1;
-        if (!ptx::mbar_wait(&sm.kv_full[slot], (it >> 1) & 1, tmo, &sm.abort)) return false;
+        const int slot = rk.at();
+        if (!ptx::mbar_wait(&sm.kv_full[slot], rk.phase, tmo, &sm.abort)) return false;
         ptx::tc_fence_after();
         const uint32_t ka = ptx::smem_addr(sm.kv[slot]);
-        const uint32_t d = tmem + kTmS + 128u * uint32_t(j & 1);
+        const uint32_t d = tmem + kTmS + uint32_t(kN) * uint32_t(j & 1);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          const uint32_t off = uint32_t(kk >> 2) * kChunkBytes + uint32_t(kk & 3) * 32u;
-          ptx::mma_ss(d, ptx::sdesc_sw128(qa + off, 16, 1024), ptx::sdesc_sw128(ka + off, 16, 1024),
+          const uint32_t qo = uint32_t(kk >> 2) * kQChunk + uint32_t(kk & 3) * 32u;
+          const uint32_t ko = uint32_t(kk >> 2) * kChunkBytes + uint32_t(kk & 3) * 32u;
+          ptx::mma_ss(d, ptx::sdesc_sw128(qa + qo, 16, 1024), ptx::sdesc_sw128(ka + ko, 16, 1024),
                       kIdescS, kk > 0);
         }
         ptx::tc_commit(&sm.s_full[j & 1]);
         ptx::tc_commit(&sm.kv_empty[slot]);
-        ++it;
+        rk.advance();
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
         if (!ptx::mbar_wait(&sm.p_full[j & 1], (j >> 1) & 1, tmo, &sm.abort)) return false;
-        const int slot = it & 1;
-        if (!ptx::mbar_wait(&sm.kv_full[slot], (it >> 1) & 1, tmo, &sm.abort)) return false;
+        const int slot = rv.at();
+        if (!ptx::mbar_wait(&sm.kv_full[slot], rv.phase, tmo, &sm.abort)) return false;
         ptx::tc_fence_after();
         const uint32_t va = ptx::smem_addr(sm.kv[slot]);
-        const uint32_t pa = tmem + kTmS + 128u * uint32_t(j & 1);
+        const uint32_t pa = tmem + kTmS + uint32_t(kN) * uint32_t(j & 1);
+        constexpr int kStepsHalf = kHalf / 16;   // k16 steps per softmax half
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acol = kk < 4 ? uint32_t(kk) * 8u : 64u + uint32_t(kk - 4) * 8u;
-          ptx::mma_ts(tmem + kTmO, pa + acol, ptx::sdesc_sw128(va + uint32_t(kk) * 2048u, 16384, 1024),
-                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kN / 16; ++kk) {
+          // P of keys 16kk..16kk+15: half kk / kStepsHalf, 8 columns per k16 step
+          const uint32_t acol = uint32_t(kk / kStepsHalf) * kHalf + uint32_t(kk % kStepsHalf) * 8u;
+          ptx::mma_ts(tmem + kTmO, pa + acol,
+                      ptx::sdesc_sw128(va + uint32_t(kk) * 2048u, kChunkBytes, 1024), kIdescPV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
         }
         ptx::tc_commit(&sm.pv_done);
         ptx::tc_commit(&sm.kv_empty[slot]);
-        ++it;
+        rv.advance();
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -265,22 +308,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const int buf = j & 1;
       bool mine = warp_all(ptx::mbar_wait(&sm.s_full[buf], (j >> 1) & 1, tmo, &sm.abort)) &&
                   !sm.abort;
-      uint32_t s[64];
+      uint32_t s[kHalf];
       float mx = -INFINITY;
       if (mine) {
         ptx::tc_fence_after();
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-        ptx::tmem_ld32_wait(trow + kTmS + 128u * buf + 64u * half, s0);
-        ptx::tmem_ld32_wait(trow + kTmS + 128u * buf + 64u * half + 32u, s1);
-        const int key0 = j * kN + half * 64;
-        if (key0 + 64 > lim) {
+        const uint32_t sa = trow + kTmS + uint32_t(kN) * buf + uint32_t(kHalf) * half;
+        if constexpr (kHalf == 64) {
+          ptx::tmem_ld64_wait(sa, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
+        } else {
+          ptx::tmem_ld32_wait(sa, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        }
+        const int key0 = j * kN + half * kHalf;
+        if (key0 + kHalf > lim) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
+          for (int c = 0; c < kHalf; ++c)
             if (key0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
         }
+        float m8[8];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int c = 0; c < 8; ++c) m8[c] = __uint_as_float(s[c]);
+#pragma unroll
+        for (int c = 8; c < kHalf; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(s[c]));
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         mx *= kScaleLog2;
       }
       sm.red[buf][half][row] = mx;
@@ -321,17 +371,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         continue;  // the next exchange stops both threads of the pair
       }
       const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      float lsum = 0.f;
-      uint32_t pk[32];
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[kHalf / 2];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < kHalf / 2; ++c) {
         const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), kScaleLog2, -msub));
         const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), kScaleLog2, -msub));
-        lsum += p0 + p1;
+        ls4[c & 3] += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
-      l_part += lsum;
-      ptx::tmem_st32_wait(trow + kTmS + 128u * buf + 64u * half, pk);
+      l_part += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+      const uint32_t pdst = trow + kTmS + uint32_t(kN) * buf + uint32_t(kHalf) * half;
+      if constexpr (kHalf == 64) {
+        ptx::tmem_st32_wait(pdst, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      } else {
+        ptx::tmem_st16_wait(pdst, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sm.p_full[buf]);
@@ -459,7 +514,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
     // Only keys a row of the call can see are addressable; TMA zero-fills the rest.
     const cuuint64_t dims[3] = {256, cuuint64_t(a.kv_offset + a.Lq), cuuint64_t(a.B) * a.Hkv};
     const cuuint64_t str[2] = {512, cuuint64_t(a.Lkv) * 512};
-    const cuuint32_t box[3] = {64, cuuint32_t(kN), 1};
+    const cuuint32_t box[3] = {64, cuuint32_t(kN), 1};   // one column block of a tile
     if (!encode_bf16(fn, &tk, a.K, 3, dims, str, box)) *encode_failed = true;
     if (!encode_bf16(fn, &tv, a.V, 3, dims, str, box)) *encode_failed = true;
   }

@@ -125,7 +125,8 @@ def test_decode_plan_rule(lib):
         assert S >= 1 and S * C >= L and (S - 1) * C < L        # no empty trailing split
         size = lib.gqa_attn_decode_workspace_size(B, T, Hq, Hkv, R, L)
         assert size == S * T * Hq * 257 * 4
-    assert plan(lib, 16, 16, 24, 4, 1, 32768)[1:] == (10, 3328)
+    assert plan(lib, 16, 16, 24, 4, 1, 32768)[1:] == (15, 2240)    # 6 x 152 CTAs / 64 units
+    assert plan(lib, 8, 68, 16, 2, 32, 65536)[1:] == (10, 6592)     # 4 x 152 / 64 units
     assert plan(lib, 0, 1, 8, 8, 1, 1)[0] == 1
     assert lib.gqa_attn_decode_workspace_size(0, 1, 8, 8, 1, 1) == 0
 
