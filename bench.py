@@ -548,6 +548,11 @@ CASES = {
     "decode_8k": lambda: S.make_decode(16, 24, 4, [1] * 16,
                                        [2048 + (b * 389) % 6145 for b in range(16)],
                                        Lcap=8192, seed=1),
+    # 8 sequences x 16/2 heads, verify rows 1..32, kv lengths a fifth of the 35B
+    # draft-verify workload's in a [8,2,16384,256] cache (268 MB)
+    "verify_16k": lambda: S.make_decode(8, 16, 2, [1, 3, 4, 8, 16, 32, 1, 3],
+                                        [4325, 854, 4593, 4238, 7757, 3758, 4011, 9102],
+                                        Lcap=16384, seed=4),
 }
 
 
@@ -564,9 +569,9 @@ def run_case(name, launches, warmup):
             G.prefill(q, k, v, g, kv_offset=x.kv_offset, out=out)
     else:
         q, kc, vc, g = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.g))
-        kv = x.kv_lens.to(dev)
+        kv, cu = x.kv_lens.to(dev), x.cu_rows.to(dev)
         for _ in range(warmup + launches):
-            G.decode(q, kc, vc, g, kv, None, max_rows=1, max_kv_len=int(x.kv_lens.max()))
+            G.decode(q, kc, vc, g, kv, cu, max_rows=max(x.rows), max_kv_len=int(x.kv_lens.max()))
     torch.cuda.synchronize()
     st = G.last_device_status()
     log(f"case {name}: {warmup + launches} launches, device status {st}")

@@ -63,9 +63,38 @@ int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 // (sequence, group, row block) units (two CTAs fit per SM up to 32 packed rows, one
 // above), so that ragged kv lengths still leave enough CTAs to balance the SMs;
 // splits are whole 64-key steps.
+// Decode / verify groups with at least this many packed rows (new rows x query heads
+// per KV group) run on the tcgen05 kernel; fewer run on the mma.sync split kernel,
+// which is memory-bound there already.
+constexpr long long kTcMinPackedRows = 64;
+constexpr int kTcMinSplitKeys = 1024;   // at least 8 key tiles per tcgen05 CTA
+
+bool tc_path(int Hq, int Hkv, int max_rows) {
+  return (long long)max_rows * (Hq / Hkv) >= kTcMinPackedRows && Hq / Hkv <= 128;
+}
+
 int plan_decode(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int num_sms, int* S,
                 int* C) {
   const int gqa = Hq / Hkv;
+  if (tc_path(Hq, Hkv, max_rows)) {
+    // tcgen05 path: one CTA per SM; aim for ~3 CTAs per SM on the longest sequence's
+    // basis (ragged lengths leave fewer live), splits of whole 128-key tiles and at
+    // least kTcMinSplitKeys keys so the prologue, the epilogue and the merge stay small.
+    const int kt = tc_split_keys_multiple();
+    const long long R = 128 / gqa;
+    const long long units = (long long)B * Hkv * ((max_rows + R - 1) / R);
+    const long long want = 3LL * num_sms;
+    long long s = (want + units - 1) / units;
+    const long long tiles = (max_kv_len + kt - 1) / kt;
+    if (s > tiles) s = tiles;
+    if (s < 1) s = 1;
+    long long c = ((max_kv_len + s - 1) / s + kt - 1) / kt * kt;
+    if (c < kTcMinSplitKeys) c = kTcMinSplitKeys;
+    s = (max_kv_len + c - 1) / c;
+    *S = int(s);
+    *C = int(c);
+    return GQA_OK;
+  }
   const long long packed = (long long)max_rows * gqa;
   const int MB = decode_rows_per_cta(int(packed > (1 << 30) ? (1 << 30) : packed));
   const long long n_rb = (packed + MB - 1) / MB;
@@ -106,6 +135,12 @@ int run_split(const void* Q, const void* Kc, const void* Vc, const int* kv_lens,
   if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
   DecodeSplitArgs a{Q, Kc, Vc, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
                     max_rows, max_kv_len, S, C};
+  if (tc_path(Hq, Hkv, max_rows) && C % tc_split_keys_multiple() == 0) {
+    bool encode_failed = false;
+    const cudaError_t e = launch_decode_split_tc(a, ctl, stream, &encode_failed);
+    if (encode_failed) return GQA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  }
   return launch_decode_split(a, ctl, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 

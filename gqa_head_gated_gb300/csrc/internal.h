@@ -44,6 +44,13 @@ int decode_rows_per_cta(int packed_rows);
 cudaError_t launch_decode_split(const DecodeSplitArgs& a, const LaunchCtl& ctl,
                                 cudaStream_t stream);
 
+// The same split on the tcgen05 kernel (split mode of the prefill kernel); split_keys
+// must be a multiple of tc_split_keys_multiple().  Sets *encode_failed when a TMA
+// descriptor could not be built.
+int tc_split_keys_multiple();
+cudaError_t launch_decode_split_tc(const DecodeSplitArgs& a, const LaunchCtl& ctl,
+                                   cudaStream_t stream, bool* encode_failed);
+
 struct MergeArgs {
   const float* O_parts;
   const float* lse_parts;

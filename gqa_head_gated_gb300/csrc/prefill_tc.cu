@@ -1,4 +1,5 @@
-// Prefill (prompt rows) of gated causal GQA attention on sm_103a tensor cores.
+// Gated causal GQA attention on sm_103a tensor cores: prompt rows (prefill) and,
+// in split mode, decode / verify rows against a KV cache over one key split.
 //
 // One CTA computes one tile of 128 packed rows: R = floor(128/GQA) consecutive
 // query rows of every query head of one KV group (row m of the tile is head
@@ -26,10 +27,24 @@
 // Softmax: fp32, base 2 with the 1/16 scale folded in; a row's running max (and
 // its O row in TMEM) is only moved when a tile raises it by more than 32, so
 // p <= 2^32 and the fp32 sums stay far from overflow (l < 2^32 x keys) while
-// rescales - a TMEM round trip of the whole O row - stay rare.  Masked keys get probability
-// exactly 0 by selection, never exp(-inf)*0 arithmetic; K/V rows past the last
-// row's horizon are zero-filled by TMA, so nothing outside the visible range is
-// ever multiplied.  Epilogue: out = O / l * sigmoid(G), rounded once to bf16.
+// rescales - a TMEM round trip of the whole O row - stay rare.  Masked keys get
+// probability exactly 0 by selection, never exp(-inf)*0 arithmetic; K/V rows past
+// the last row's horizon are zero-filled by TMA, so nothing outside the visible
+// range is ever multiplied.
+// Epilogue: out = O / l * sigmoid(G), rounded once to bf16.
+//
+// Split mode (decode / chain verify, TensorFold PR #1009 "Receipt": decode over cache
+// chunks whose partial results are merged): one CTA takes R = floor(128/GQA) new
+// tokens x all GQA heads of one (sequence, KV group) - row m is token m / GQA, head
+// m % GQA, matching the token-major [T, Hq, 256] layout - against the keys of one
+// split [k_lo, k_hi), k_lo a multiple of kN.  Sequence lengths live on the device,
+// so the cache tensor map spans the whole capacity: K columns past kv_len are
+// masked by selection, and the producer warp zeroes the V rows past kv_len of the
+// CTA's last tile (its last copy) in shared memory before the last PV may start, so
+// cache padding (any bits, NaN included) never meets a zero probability inside the
+// MMA.  The epilogue writes the normalised
+// partial O / l (fp32) and lse = m + ln l for attn_lse_merge, or lse = -inf for a
+// row that sees no key of the split.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -82,6 +97,7 @@ struct __align__(1024) Smem {
   uint64_t pv_done;
   uint64_t o_final;
   uint64_t drain;
+  uint64_t v_clean;            // split mode: the last V tile's padding rows are zeroed
   uint32_t tmem_base;
   int abort;
   int zero;
@@ -94,6 +110,12 @@ struct Params {
   __nv_bfloat16* out;
   float* lse;
   int B, Hq, Hkv, Lq, kv_offset, gqa, R, n_rtiles;
+  // split mode
+  const int* kv_lens;
+  const int* cu_rows;
+  float* O_parts;
+  float* lse_parts;
+  int T, Lcap, max_rows, max_kv_len, split_keys, num_splits;
   LaunchCtl ctl;
 };
 
@@ -140,25 +162,66 @@ __device__ __forceinline__ void item_kind(int it, int n, bool& is_v, int& j) {
   }
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  const int BH = p.B * p.Hkv;
-  const int rt = p.n_rtiles - 1 - static_cast<int>(blockIdx.x) / BH;   // longest first
-  const int bg = static_cast<int>(blockIdx.x) % BH;
-  const int b = bg / p.Hkv;
-  const int g = bg % p.Hkv;
-  const int r0 = rt * p.R;
-  const int rows_here = min(p.R, p.Lq - r0);
-  const int n_keys = p.kv_offset + r0 + rows_here;   // keys the last row of the tile sees
-  const int n_tiles = (n_keys + kN - 1) / kN;
   const uint64_t tmo = p.ctl.timeout_ns;
+
+  int b, g, r0, rows_here, n_tiles, j0 = 0, bg;
+  // split mode only
+  int s_idx = 0, t0 = 0, rows = 0, kv_len = 0, k_hi = 0, n_hi = 0;
+  if constexpr (!kSplit) {
+    const int BH = p.B * p.Hkv;
+    const int rt = p.n_rtiles - 1 - static_cast<int>(blockIdx.x) / BH;   // longest first
+    bg = static_cast<int>(blockIdx.x) % BH;
+    b = bg / p.Hkv;
+    g = bg % p.Hkv;
+    r0 = rt * p.R;
+    rows_here = min(p.R, p.Lq - r0);
+    const int n_keys = p.kv_offset + r0 + rows_here;   // keys the last row of the tile sees
+    n_tiles = (n_keys + kN - 1) / kN;
+  } else {
+    int bid = static_cast<int>(blockIdx.x);
+    const int rt = bid % p.n_rtiles;
+    bid /= p.n_rtiles;
+    s_idx = bid % p.num_splits;
+    bid /= p.num_splits;
+    g = bid % p.Hkv;
+    b = bid / p.Hkv;
+    bg = b * p.Hkv + g;
+    kv_len = p.kv_lens[b];
+    t0 = p.cu_rows ? p.cu_rows[b] : b;
+    const int t1 = p.cu_rows ? p.cu_rows[b + 1] : b + 1;
+    rows = t1 - t0;
+    if (rows < 0 || rows > p.max_rows || t0 < 0 || t1 > p.T || kv_len > p.max_kv_len ||
+        kv_len > p.Lcap || kv_len < rows) {
+      if (threadIdx.x == 0 && rt == 0 && s_idx == 0 && g == 0)
+        record_status(p.ctl.status, GQA_ERR_DEVICE_RANGE);
+      return;
+    }
+    r0 = rt * p.R;                        // first new token of the tile (within the sequence)
+    if (r0 >= rows) return;
+    rows_here = min(p.R, rows - r0);
+    const int k_lo = s_idx * p.split_keys;
+    k_hi = min(k_lo + p.split_keys, kv_len);
+    n_hi = min(k_hi, kv_len - rows + r0 + rows_here);   // keys the tile's last row sees
+    if (n_hi <= k_lo) {
+      // No row of the tile sees a key of this split: empty parts.
+      for (int m = threadIdx.x; m < rows_here * p.gqa; m += kThreads) {
+        const size_t n = size_t(t0 + r0 + m / p.gqa) * p.Hq + size_t(g) * p.gqa + m % p.gqa;
+        p.lse_parts[size_t(s_idx) * size_t(p.T) * p.Hq + n] = -INFINITY;
+      }
+      return;
+    }
+    j0 = k_lo / kN;
+    n_tiles = (n_hi + kN - 1) / kN - j0;
+  }
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&sm.q_full, 1);
@@ -173,6 +236,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     ptx::mbar_init(&sm.pv_done, 1);
     ptx::mbar_init(&sm.o_final, 1);
     ptx::mbar_init(&sm.drain, 1);
+    ptx::mbar_init(&sm.v_clean, 1);
     sm.abort = 0;
     sm.zero = 0;
     ptx::fence_mbar_init();
@@ -188,17 +252,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    Ring rk{0, 0u, 0, kKS, 0};
+    Ring rv{0, 0u, 0, kVS, kKS};
+    bool issued_all = false;
     if (lane == 0) {
       ptx::prefetch_tmap(&tmQ);
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
       const uint32_t q_bytes = 4u * 128u * uint32_t(p.R * p.gqa);
       ptx::mbar_arrive_expect_tx(&sm.q_full, q_bytes);
-      for (int dc = 0; dc < 4; ++dc)
-        ptx::tma_load_4d(sm.q + dc * kQChunk, &tmQ, &sm.q_full, dc * 64, r0, g * p.gqa, b);
+      for (int dc = 0; dc < 4; ++dc) {
+        if constexpr (!kSplit)
+          ptx::tma_load_4d(sm.q + dc * kQChunk, &tmQ, &sm.q_full, dc * 64, r0, g * p.gqa, b);
+        else
+          ptx::tma_load_3d(sm.q + dc * kQChunk, &tmQ, &sm.q_full, dc * 64, g * p.gqa, t0 + r0);
+      }
       const int total = 2 * n_tiles;
-      Ring rk{0, 0u, 0, kKS, 0};
-      Ring rv{0, 0u, 0, kVS, kKS};
       for (int it = 0; it < total; ++it) {
         bool is_v;
         int j;
@@ -213,11 +282,46 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         ptx::mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
         const CUtensorMap* tm = is_v ? &tmV : &tmK;
         for (int dc = 0; dc < 4; ++dc)
-          ptx::tma_load_3d(sm.kv[slot] + dc * kChunkBytes, tm, &sm.kv_full[slot], dc * 64, j * kN,
-                           bg);
+          ptx::tma_load_3d(sm.kv[slot] + dc * kChunkBytes, tm, &sm.kv_full[slot], dc * 64,
+                           (j0 + j) * kN, bg);
         r.advance();
       }
-      // Let every copy this thread started land before the CTA can exit.
+      issued_all = rv.count == n_tiles;
+    }
+    if constexpr (kSplit) {
+      // Split mode: a tile holding cache rows at or past kv_len can only be the CTA's
+      // last one, and its V copy is the last copy this warp issued.  That copy is use
+      // u of its slot and use u-1 has landed (its slot was released before the copy
+      // was issued), so the parity wait below is unambiguous.  Zero the padded rows,
+      // make the writes visible to the tensor core, then release the last PV.
+      const int jl = n_tiles - 1;
+      const int tile_key0 = (j0 + jl) * kN;
+      if (tile_key0 + kN > kv_len) {
+        const int vslot = kKS + jl % kVS;
+        const bool go = __shfl_sync(0xffffffffu, issued_all ? 1 : 0, 0) != 0;
+        const bool landed =
+            go && warp_all(ptx::mbar_wait(&sm.kv_full[vslot], uint32_t(jl / kVS) & 1u, tmo,
+                                          &sm.abort));
+        if (landed) {
+          const int r_first = max(0, kv_len - tile_key0);
+          const int per_blk = (kN - r_first) * 8;   // 16-byte chunks per column block
+          uint4* base = reinterpret_cast<uint4*>(sm.kv[vslot]);
+          for (int c = lane; c < 4 * per_blk; c += 32) {
+            const int blk = c / per_blk;
+            const int rem = c - blk * per_blk;
+            base[(blk * kChunkBytes + (r_first + rem / 8) * 128) / 16 + rem % 8] =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          ptx::fence_proxy_async_smem();
+        } else if (lane == 0) {
+          fail(sm, p);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.v_clean);
+      }
+    }
+    if (lane == 0) {
+      // Let every copy this warp started land before the CTA can exit.
       for (Ring* r : {&rk, &rv})
         for (int c = max(0, r->count - r->n); c < r->count; ++c)
           ptx::mbar_wait(&sm.kv_full[r->base + c % r->n], uint32_t(c / r->n) & 1u, tmo, &sm.zero);
@@ -254,6 +358,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (!ptx::mbar_wait(&sm.p_full[j & 1], (j >> 1) & 1, tmo, &sm.abort)) return false;
         const int slot = rv.at();
         if (!ptx::mbar_wait(&sm.kv_full[slot], rv.phase, tmo, &sm.abort)) return false;
+        if constexpr (kSplit) {
+          if (j == n_tiles - 1 && (j0 + j) * kN + kN > kv_len &&
+              !ptx::mbar_wait(&sm.v_clean, 0, tmo, &sm.abort))
+            return false;
+        }
         ptx::tc_fence_after();
         const uint32_t va = ptx::smem_addr(sm.kv[slot]);
         const uint32_t pa = tmem + kTmS + uint32_t(kN) * uint32_t(j & 1);
@@ -294,11 +403,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int lq = warp & 3;
     const int row = lq * 32 + lane;
     const uint32_t bar_id = 1 + lq;
-    const int hh = row / p.R;
-    const int rr = row - hh * p.R;
-    const bool valid = (row < p.R * p.gqa) && (r0 + rr < p.Lq);
+    int hh, rr, lim;
+    bool valid;
+    if constexpr (!kSplit) {
+      hh = row / p.R;                     // row m: head m / R, prompt row r0 + m % R
+      rr = row - hh * p.R;
+      valid = (row < p.R * p.gqa) && (r0 + rr < p.Lq);
+      lim = valid ? p.kv_offset + r0 + rr + 1 : p.kv_offset + r0 + 1;
+    } else {
+      rr = row / p.gqa;                   // row m: token r0 + m / GQA, head m % GQA
+      hh = row - rr * p.gqa;
+      valid = (row < p.R * p.gqa) && (rr < rows_here);
+      lim = valid ? min(kv_len - rows + r0 + rr + 1, k_hi) : n_hi;
+    }
     const int q = r0 + rr;
-    const int lim = valid ? p.kv_offset + q + 1 : p.kv_offset + r0 + 1;
     const uint32_t trow = tmem + (uint32_t(lq * 32) << 16);
 
     float m_run = -INFINITY;
@@ -318,7 +436,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         } else {
           ptx::tmem_ld32_wait(sa, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         }
-        const int key0 = j * kN + half * kHalf;
+        const int key0 = (j0 + j) * kN + half * kHalf;
         if (key0 + kHalf > lim) {
 #pragma unroll
           for (int c = 0; c < kHalf; ++c)
@@ -404,50 +522,73 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       ptx::tc_fence_after();
       const float l_tot = l_part + sm.red[pb][half ^ 1][row];
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const int h = g * p.gqa + hh;
-      const size_t row_off = (size_t(b) * p.Hq + h) * size_t(p.Lq) + size_t(q);
+      if constexpr (!kSplit) {
+        const int h = g * p.gqa + hh;
+        const size_t row_off = (size_t(b) * p.Hq + h) * size_t(p.Lq) + size_t(q);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t o[32];
-        ptx::tmem_ld32_wait(trow + kTmO + 128u * half + 32u * cc, o);
-        if (valid) {
-          const int col0 = half * 128 + cc * 32;
-          float gs[32];
-          if (p.G != nullptr) {
-            const uint4* gp = reinterpret_cast<const uint4*>(p.G + row_off * kHeadDim + col0);
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          ptx::tmem_ld32_wait(trow + kTmO + 128u * half + 32u * cc, o);
+          if (valid) {
+            const int col0 = half * 128 + cc * 32;
+            float gs[32];
+            if (p.G != nullptr) {
+              const uint4* gp = reinterpret_cast<const uint4*>(p.G + row_off * kHeadDim + col0);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const uint4 u = __ldg(gp + v);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = unpack_bf16x2(w[e]);
+                  gs[v * 8 + 2 * e] = gate_sigmoid(f.x);
+                  gs[v * 8 + 2 * e + 1] = gate_sigmoid(f.y);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) gs[c] = 1.f;
+            }
+            uint4* op = reinterpret_cast<uint4*>(p.out + row_off * kHeadDim + col0);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              const uint4 u = __ldg(gp + v);
-              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = unpack_bf16x2(w[e]);
-                gs[v * 8 + 2 * e] = gate_sigmoid(f.x);
-                gs[v * 8 + 2 * e + 1] = gate_sigmoid(f.y);
-              }
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(o[v * 8 + 0]) * inv_l * gs[v * 8 + 0],
+                                __uint_as_float(o[v * 8 + 1]) * inv_l * gs[v * 8 + 1]);
+              u.y = pack_bf16x2(__uint_as_float(o[v * 8 + 2]) * inv_l * gs[v * 8 + 2],
+                                __uint_as_float(o[v * 8 + 3]) * inv_l * gs[v * 8 + 3]);
+              u.z = pack_bf16x2(__uint_as_float(o[v * 8 + 4]) * inv_l * gs[v * 8 + 4],
+                                __uint_as_float(o[v * 8 + 5]) * inv_l * gs[v * 8 + 5]);
+              u.w = pack_bf16x2(__uint_as_float(o[v * 8 + 6]) * inv_l * gs[v * 8 + 6],
+                                __uint_as_float(o[v * 8 + 7]) * inv_l * gs[v * 8 + 7]);
+              op[v] = u;
             }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) gs[c] = 1.f;
-          }
-          uint4* op = reinterpret_cast<uint4*>(p.out + row_off * kHeadDim + col0);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(o[v * 8 + 0]) * inv_l * gs[v * 8 + 0],
-                              __uint_as_float(o[v * 8 + 1]) * inv_l * gs[v * 8 + 1]);
-            u.y = pack_bf16x2(__uint_as_float(o[v * 8 + 2]) * inv_l * gs[v * 8 + 2],
-                              __uint_as_float(o[v * 8 + 3]) * inv_l * gs[v * 8 + 3]);
-            u.z = pack_bf16x2(__uint_as_float(o[v * 8 + 4]) * inv_l * gs[v * 8 + 4],
-                              __uint_as_float(o[v * 8 + 5]) * inv_l * gs[v * 8 + 5]);
-            u.w = pack_bf16x2(__uint_as_float(o[v * 8 + 6]) * inv_l * gs[v * 8 + 6],
-                              __uint_as_float(o[v * 8 + 7]) * inv_l * gs[v * 8 + 7]);
-            op[v] = u;
           }
         }
+        if (valid && half == 0 && p.lse != nullptr)
+          p.lse[row_off] = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
+      } else {
+        // Normalised partial O / l (fp32) and lse for the merge; -inf: no key seen.
+        const size_t n = size_t(t0 + q) * p.Hq + size_t(g) * p.gqa + hh;
+        const size_t part = size_t(s_idx) * size_t(p.T) * p.Hq + n;
+        const bool live = valid && l_tot > 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          ptx::tmem_ld32_wait(trow + kTmO + 128u * half + 32u * cc, o);
+          if (live) {
+            float4* op =
+                reinterpret_cast<float4*>(p.O_parts + part * kHeadDim + half * 128 + cc * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              op[v] = make_float4(
+                  __uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                  __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          }
+        }
+        if (valid && half == 0)
+          p.lse_parts[part] = live ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
       }
-      if (valid && half == 0 && p.lse != nullptr)
-        p.lse[row_off] = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
     } else {
       fail(sm, p);
     }
@@ -520,7 +661,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
   }
   if (*encode_failed) return cudaErrorInvalidValue;
 
-  Params p;
+  Params p{};
   p.G = static_cast<const __nv_bfloat16*>(a.G);
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
@@ -535,15 +676,68 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
   p.ctl = ctl;
 
   const size_t smem = sizeof(Smem) + 1024;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    int(smem));
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
   const long long grid = (long long)p.n_rtiles * a.B * a.Hkv;
-  prefill_kernel<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
+  attn_tc_kernel<false><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+int tc_split_keys_multiple() { return kN; }
+
+cudaError_t launch_decode_split_tc(const DecodeSplitArgs& a, const LaunchCtl& ctl,
+                                   cudaStream_t stream, bool* encode_failed) {
+  *encode_failed = false;
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) {
+    *encode_failed = true;
+    return cudaErrorNotSupported;
+  }
+  const int gqa = a.Hq / a.Hkv;
+  const int R = prefill_rows_per_tile(gqa);
+  CUtensorMap tq, tk, tv;
+  {
+    // Q [T, Hq, 256]: a box is R tokens x the group's GQA heads x 64 dims.
+    const cuuint64_t dims[3] = {256, cuuint64_t(a.Hq), cuuint64_t(a.T)};
+    const cuuint64_t str[2] = {512, cuuint64_t(a.Hq) * 512};
+    const cuuint32_t box[3] = {64, cuuint32_t(gqa), cuuint32_t(R)};
+    if (!encode_bf16(fn, &tq, a.Q, 3, dims, str, box)) *encode_failed = true;
+  }
+  {
+    const cuuint64_t dims[3] = {256, cuuint64_t(a.Lcap), cuuint64_t(a.B) * a.Hkv};
+    const cuuint64_t str[2] = {512, cuuint64_t(a.Lcap) * 512};
+    const cuuint32_t box[3] = {64, cuuint32_t(kN), 1};
+    if (!encode_bf16(fn, &tk, a.K, 3, dims, str, box)) *encode_failed = true;
+    if (!encode_bf16(fn, &tv, a.V, 3, dims, str, box)) *encode_failed = true;
+  }
+  if (*encode_failed) return cudaErrorInvalidValue;
+
+  Params p{};
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.gqa = gqa;
+  p.R = R;
+  p.n_rtiles = (a.max_rows + R - 1) / R;
+  p.kv_lens = a.kv_lens;
+  p.cu_rows = a.cu_rows;
+  p.O_parts = a.O_parts;
+  p.lse_parts = a.lse_parts;
+  p.T = a.T;
+  p.Lcap = a.Lcap;
+  p.max_rows = a.max_rows;
+  p.max_kv_len = a.max_kv_len;
+  p.split_keys = a.split_keys;
+  p.num_splits = a.num_splits;
+  p.ctl = ctl;
+
+  const size_t smem = sizeof(Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)a.B * a.Hkv * a.num_splits * p.n_rtiles;
+  attn_tc_kernel<true><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -131,6 +131,10 @@ int gqa_attn_decode_plan(int B, int T, int Hq, int Hkv, int max_rows, int max_kv
  * Row n of the parts is output row (t, h) with n = t*Hq + h.
  * num_splits >= 1 and split_keys (a positive multiple of 64) with
  * num_splits*split_keys >= max_kv_len; gqa_attn_decode_plan() gives the defaults.
+ * Kernel: when a KV group packs at least 64 rows (max_rows x Hq/Hkv >= 64) and
+ * split_keys is a multiple of 128, the split runs on tcgen05 tensor cores (TMEM
+ * accumulators, TMA-staged tiles); otherwise on an mma.sync kernel with 16-byte
+ * cp.async cache reads.  Both give the same partial results up to rounding.
  */
 int gqa_attn_decode_split(const void* Q, const void* Kcache, const void* Vcache,
                           const int* kv_lens, const int* cu_rows, float* O_parts,

@@ -126,7 +126,10 @@ def test_decode_plan_rule(lib):
         size = lib.gqa_attn_decode_workspace_size(B, T, Hq, Hkv, R, L)
         assert size == S * T * Hq * 257 * 4
     assert plan(lib, 16, 16, 24, 4, 1, 32768)[1:] == (15, 2240)    # 6 x 152 CTAs / 64 units
-    assert plan(lib, 8, 68, 16, 2, 32, 65536)[1:] == (10, 6592)     # 4 x 152 / 64 units
+    # 32 rows x 8 heads per group: tcgen05 path, 3 x 152 CTAs / (8 x 2 x 2 row tiles),
+    # whole 128-key tiles
+    assert plan(lib, 8, 68, 16, 2, 32, 65536)[1:] == (15, 4480)
+    assert plan(lib, 1, 8, 8, 1, 8, 5000)[1:] == (5, 1024)           # at least 1024 keys
     assert plan(lib, 0, 1, 8, 8, 1, 1)[0] == 1
     assert lib.gqa_attn_decode_workspace_size(0, 1, 8, 8, 1, 1) == 0
 
