@@ -19,7 +19,8 @@ from ._lib import GqaError, check, load  # noqa: F401
 HEAD_DIM = 256
 
 __all__ = ["prefill", "decode", "decode_plan", "decode_split", "lse_merge",
-           "decode_workspace_size", "last_device_status", "set_wait_timeout_ns", "GqaError",
+           "decode_workspace_size", "last_device_status", "set_wait_timeout_ns",
+           "selftest_wait_timeout", "GqaError",
            "load"]
 
 
@@ -166,3 +167,13 @@ def last_device_status():
 
 def set_wait_timeout_ns(ns):
     load().gqa_set_wait_timeout_ns(int(ns))
+
+
+def selftest_wait_timeout():
+    """Runs the kernels' bounded wait on a barrier nothing completes.  Returns
+    (device status, nanoseconds the wait took); the status should be
+    GQA_ERR_TIMEOUT (4) and the time about the configured bound."""
+    el = torch.zeros(1, dtype=torch.int64, device="cuda")
+    check(load().gqa_selftest_wait_timeout(_ptr(el), _stream()), "gqa_selftest_wait_timeout")
+    st = last_device_status()
+    return st, int(el.item())

@@ -195,6 +195,17 @@ int gqa_last_device_status(gqa_stream_t stream);
  */
 void gqa_set_wait_timeout_ns(unsigned long long ns);
 
+/*
+ * Failure-detection self test.  Launches one warp that runs the kernels' bounded
+ * spin wait (the same code every mbarrier wait in the kernels uses) on a barrier
+ * that nothing completes.  After the bound (gqa_set_wait_timeout_ns) it records
+ * GQA_ERR_TIMEOUT in the device status word and returns; the context stays usable.
+ * elapsed_ns: NULL, or a device pointer (8-byte aligned) that receives the time
+ * the wait took, from the global timer.  Returns GQA_ERR_CUDA if the launch fails.
+ * Read the outcome with gqa_last_device_status().
+ */
+int gqa_selftest_wait_timeout(unsigned long long* elapsed_ns, gqa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
