@@ -56,6 +56,23 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# ----------------------------------------------------------------------------- traffic
+def dram_traffic(kernel, units):
+    """DRAM bytes per launch for `kernel` on a workload of `units`, scaled from the
+    ncu capture recorded in profiles/dram_traffic.json; None when there is no record
+    or the kernel's source changed since the capture (hash mismatch)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+                return None
+    except (OSError, KeyError, ValueError):
+        return None
+    return round((rec["dram_read"] + rec["dram_write"]) * units / rec["units"])
+
+
 # ----------------------------------------------------------------------------- work counts
 def decode_bytes(x):
     """Algorithmic bytes of one decode call: K and V of every key a sequence holds
@@ -254,16 +271,21 @@ def oracle_decode_sample(x, budget_s=10.0, min_seqs=1):
 
 
 # ----------------------------------------------------------------------------- our arm
-def setup_decode(x, steps, dev):
+def setup_decode(x, steps, dev, with_rows=False):
+    """Device copies and the split plan of a decode (one row per sequence) or, with
+    `with_rows`, a verify workload (cu_rows passed to the kernels)."""
     import gqa_head_gated_gb300 as G
     q, kc, vc, g = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.g))
     kv = x.kv_lens.to(dev)
+    cu = x.cu_rows.to(dev) if with_rows else None
+    max_rows = max(x.rows) if with_rows else 1
     B, Hkv = kc.shape[0], kc.shape[1]
     T, Hq = q.shape[0], q.shape[1]
     max_kv = int(x.kv_lens.max())
-    S_, C_ = G.decode_plan(B, T, Hq, Hkv, 1, max_kv)
+    S_, C_ = G.decode_plan(B, T, Hq, Hkv, max_rows, max_kv)
     ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
-    return dict(q=q, kc=kc, vc=vc, g=g, kv=kv, max_kv=max_kv, plan=(S_, C_), ev=ev,
+    return dict(q=q, kc=kc, vc=vc, g=g, kv=kv, cu=cu, max_rows=max_rows, max_kv=max_kv,
+                plan=(S_, C_), ev=ev,
                 op=torch.empty((S_, T * Hq, 256), dtype=torch.float32, device=dev),
                 lp=torch.empty((S_, T * Hq), dtype=torch.float32, device=dev),
                 out=torch.empty_like(q), flush=L2Flush(dev))
@@ -279,7 +301,7 @@ def run_decode_timed(ctx, steps):
         ctx["flush"]()
         a, m, b = ctx["ev"][i % len(ctx["ev"])]
         a.record()
-        G.decode_split(q, kc, vc, kv, None, max_rows=1, max_kv_len=ctx["max_kv"],
+        G.decode_split(q, kc, vc, kv, ctx["cu"], max_rows=ctx["max_rows"], max_kv_len=ctx["max_kv"],
                        num_splits=S_, split_keys=C_, o_parts=ctx["op"], lse_parts=ctx["lp"])
         m.record()
         G.lse_merge(ctx["op"], ctx["lp"], ctx["g"], out=ctx["out"].view(-1, 256))
@@ -330,7 +352,7 @@ def bench_e2e_decode(x, steps, warmup, dev):
     return sum(times), h2d, d2h, ok
 
 
-def bench_prefill(x, steps, warmup, dev):
+def bench_prefill(x, steps, warmup, dev, e2e=True):
     import gqa_head_gated_gb300 as G
     q, k, v, g = (t.to(dev) for t in (x.q, x.k, x.v, x.g))
     out = torch.empty_like(q)
@@ -351,6 +373,8 @@ def bench_prefill(x, steps, warmup, dev):
         torch.cuda.synchronize()
     status = G.last_device_status()
     ms = elapsed_ms(pairs)
+    if not e2e:
+        return ms, status, None, None, None, clk.summary()
     # e2e: host buffers in, out back
     hq, hk, hv, hg = (t.pin_memory() for t in (x.q, x.k, x.v, x.g))
     hout = torch.empty_like(x.q).pin_memory()
@@ -420,6 +444,40 @@ def ours(args):
     bf16_peak = float(peaks["bf16_tflops"])
     pf_e2e_avg = sum(pf_e2e) / len(pf_e2e)
 
+    # the other throughput workloads of the metric, inside the same line
+    more = {}
+    if not args.no_extra:
+        cp = S.chunked_prefill_35b()
+        cp_flops = prefill_flops(cp)
+        cp_ms = bench_prefill(cp, pf_steps, max(3, args.warmup), dev, e2e=False)[0]
+        cp_avg = sum(cp_ms) / len(cp_ms)
+        more["chunked_prefill_35b"] = {
+            "workload": "35B-A3B chunked prefill: B=1, Hq=16, Hkv=2, 2048 rows at kv_offset "
+                        "30720 (Lkv 32768) causal, seed 3",
+            "value": round(cp_flops / (cp_avg / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+            "frac_of_bf16_peak": round(cp_flops / (cp_avg / 1e3) / 1e12 / float(peaks["bf16_tflops"]), 4),
+            "avg_ms": round(cp_avg, 4)}
+        del cp
+        vx = S.verify_35b()
+        v_kv, v_bytes = decode_bytes(vx)
+        vctx = setup_decode(vx, args.steps, dev, with_rows=True)
+        run_decode_timed(vctx, args.warmup)
+        torch.cuda.synchronize()
+        run_decode_timed(vctx, args.steps)
+        torch.cuda.synchronize()
+        v_split = sum(a.elapsed_time(m) for a, m, b in vctx["ev"]) / args.steps
+        v_step = sum(a.elapsed_time(b) for a, m, b in vctx["ev"]) / args.steps
+        more["verify_35b"] = {
+            "workload": "35B-A3B draft verify: B=8, Hq=16, Hkv=2, rows [1,3,4,8,16,32,1,3], "
+                        "kv_lens 4271..45513 in a [8,2,65536,256] cache, seed 4",
+            "value": round(v_bytes / (v_step / 1e3) / 1e9, 2), "unit": "GB/s",
+            "frac_of_hbm": round(v_bytes / (v_step / 1e3) / 1e9 / hbm_peak, 4),
+            "split_kernel_gbs": round((v_kv + vx.q.numel() * 2) / (v_split / 1e3) / 1e9, 2),
+            "split_plan": {"num_splits": vctx["plan"][0], "split_keys": vctx["plan"][1]},
+            "ms_per_step": round(v_step, 5)}
+        del vctx, vx
+        torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0:
         gbs, secs, desc = oracle_decode_sample(x, budget_s=args.cpu_budget)
@@ -459,7 +517,8 @@ def ours(args):
                 "peak_source": f"{peak_src} hbm_gbs",
                 "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4),
-                "traffic": args.traffic,
+                "traffic": args.traffic if args.traffic is not None else
+                dram_traffic("decode_split_kernel", int(x.kv_lens.sum()) * x.k_cache.shape[1]),
                 "avg_launch_ms": round(split_avg, 5),
                 "algorithmic_bytes_per_launch": split_bytes,
             },
@@ -478,16 +537,20 @@ def ours(args):
                 "flops_per_call": flops,
                 "avg_ms": round(pf_avg, 4),
                 "steps": pf_steps,
-                "roofline": {"kernel": "prefill_kernel", "bound": "tensor",
+                "roofline": {"kernel": "attn_tc_kernel<prefill>", "bound": "tensor",
                              "achieved": round(pf_tflops, 2), "peak": bf16_peak,
                              "peak_source": f"{peak_src} bf16_tflops (burst)",
                              "unit": "TFLOP/s", "frac": round(pf_tflops / bf16_peak, 4),
-                             "traffic": args.prefill_traffic},
+                             "traffic": args.prefill_traffic if args.prefill_traffic is not None
+                             else dram_traffic("attn_tc_kernel_prefill",
+                                               (pf.q.numel() + pf.k.numel() + pf.v.numel() +
+                                                pf.g.numel()) * 2)},
                 "e2e": {"value": round(flops / (pf_e2e_avg / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                         "h2d_bytes_per_step": pf_h2d, "d2h_bytes_per_step": pf_d2h},
                 "device_status": pf_status,
                 "clocks": pf_clk,
             },
+            "more_workloads": more,
             "clocks": clk.summary(),
             "device_status": status,
             "outputs_finite": out_ok and e2e_ok,
@@ -592,6 +655,8 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per split launch from an ncu capture of this kernel")
     ap.add_argument("--prefill-traffic", type=float, default=None)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 35B chunked-prefill and draft-verify measurements")
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="only launch this small case (for ncu captures); no JSON line")
     args = ap.parse_args()
