@@ -33,6 +33,8 @@ Readings where the pages are silent (each listed in the design notes):
     j <= kv_offset + i;
   * decode/verify: kv_lens[b] counts the verify rows, row i of r_b rows sees
     keys j < kv_lens[b] - r_b + i + 1;
+  * tree verify: row i sees the keys before the new rows plus the new keys its
+    mask selects (bit k = new row k); a chain is the mask of bits 0..i;
   * a row that sees no key outputs zeros and lse = -inf (float64 would give 0/0);
   * keys a row does not see are excluded from its sums: the row's key range is
     sliced, and inside a block of rows a key another row of the block sees gets
@@ -188,6 +190,60 @@ def decode(Q, Kc, Vc, G, kv_lens, cu_rows=None, rows=None):
             out[ts[0]:ts[-1] + 1, h] = o
             lse[ts[0]:ts[-1] + 1, h] = s
     return out, lse
+
+
+def tree_visible_keys(i, rows, kv_len, mask):
+    """Keys new row i (0-based of `rows`) sees under a tree mask: every key before
+    the new rows (positions < kv_len - rows) and the new key at position
+    kv_len - rows + k for each set bit k of `mask` (an integer; bit k = new row k)."""
+    base = kv_len - rows
+    return list(range(base)) + [base + k for k in range(rows) if (int(mask) >> k) & 1]
+
+
+def decode_tree(Q, Kc, Vc, G, kv_lens, cu_rows, tree_masks, rows=None):
+    """Draft verify over a token tree.  Like decode(), but new row i of a sequence
+    sees the new keys that its mask selects (its ancestors and itself) instead of
+    all earlier new keys.  tree_masks [T]: integer masks over the sequence's new
+    rows.  A chain (mask of row i = bits 0..i) gives decode()'s result.  Keys a row
+    does not see are excluded from its sums (gathered out, never multiplied)."""
+    T, Hq, D = Q.shape
+    B, Hkv = Kc.shape[0], Kc.shape[1]
+    cu = [int(x) for x in cu_rows]
+    assert D == HEAD_DIM and Hq % Hkv == 0 and cu[-1] == T
+    want = None if rows is None else list(rows)
+    out = np.zeros((T, Hq, D)) if want is None else np.zeros((len(want), D))
+    lse = np.zeros((T, Hq)) if want is None else np.zeros(len(want))
+    index = {}
+    if want is not None:
+        for n, th in enumerate(want):
+            index.setdefault(th[0], []).append((n, th[1]))
+    for b in range(B):
+        r = cu[b + 1] - cu[b]
+        L = int(kv_lens[b])
+        for i in range(r):
+            t = cu[b] + i
+            if want is not None and t not in index:
+                continue
+            keys = np.asarray(tree_visible_keys(i, r, L, tree_masks[t]), dtype=np.int64)
+            heads = range(Hq) if want is None else [h for _, h in index[t]]
+            for h in heads:
+                g = kv_head_of(h, Hq, Hkv)
+                Kg = np.asarray(Kc[b, g], dtype=np.float64)[keys]
+                Vg = np.asarray(Vc[b, g], dtype=np.float64)[keys]
+                o, l = attend_rows(np.asarray(Q[t, h:h + 1], dtype=np.float64), Kg, Vg,
+                                   None if G is None else G[t, h:h + 1], [len(keys)])
+                if want is None:
+                    out[t, h], lse[t, h] = o[0], l[0]
+                else:
+                    for n, hh in index[t]:
+                        if hh == h:
+                            out[n], lse[n] = o[0], l[0]
+    return out, lse
+
+
+def chain_masks(rows_per_seq):
+    """Masks of chain verify: new row i sees new rows 0..i."""
+    return [(1 << (i + 1)) - 1 for r in rows_per_seq for i in range(r)]
 
 
 def lse_merge(O_parts, lse_parts, G=None):

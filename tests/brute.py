@@ -80,3 +80,29 @@ def decode(Q, Kc, Vc, G, kv_lens, rows):
                 out[(t, h)] = (o, lse)
             t += 1
     return out
+
+
+def decode_tree(Q, Kc, Vc, G, kv_lens, rows, masks):
+    """Tree verify, brute force: row i of a sequence with r new rows at positions
+    L-r .. L-1 sees position p when p is before the new rows, or when p is new and
+    the mask bit of its new-row index is set."""
+    Hq = len(Q[0])
+    Hkv = len(Kc[0])
+    out = {}
+    t = 0
+    for b, r in enumerate(rows):
+        L = int(kv_lens[b])
+        for i in range(r):
+            m = int(masks[t])
+            seen = []
+            for p in range(L):
+                new_index = p - (L - r)
+                if new_index < 0 or (m >> new_index) % 2 == 1:
+                    seen.append(p)
+            for h in range(Hq):
+                kvh = (h * Hkv) // Hq
+                o, lse = _row(Q[t][h], [Kc[b][kvh][p] for p in seen],
+                              [Vc[b][kvh][p] for p in seen], None if G is None else G[t][h])
+                out[(t, h)] = (o, lse)
+            t += 1
+    return out

@@ -32,6 +32,11 @@ MUTANTS = {
                               "live = [s for s in range(S) if np.isfinite(lse_parts[s, n])][:-1]"),
     "merge ignores weights": ("acc += ws * O_parts[s, n]", "acc += O_parts[s, n]"),
     "plan drops remainder": ("    if gqa % c:\n        plan.append(gqa % c)\n", ""),
+    "tree: new rows start one key late": ("    base = kv_len - rows\n    return list(range(base))",
+                                          "    base = kv_len - rows + 1\n    return list(range(base))"),
+    "tree: mask bits shifted": ("if (int(mask) >> k) & 1]", "if (int(mask) >> (k + 1)) & 1]"),
+    "tree: self bit ignored": ("for k in range(rows) if (int(mask) >> k) & 1]",
+                               "for k in range(rows) if (int(mask) >> k) & 1 and k != i]"),
     "plan chunk one head too wide": ("c = min(gqa, limit // rows)", "c = min(gqa, limit // rows + 1)"),
     "plan ignores the row bound": ("rows > limit or ", ""),
 }

@@ -290,12 +290,72 @@ def check_plan_golden(ora):
     return ""
 
 
+def _tree_masks(rows, seed):
+    """Random token trees: new row i's parent is a random earlier row (or none);
+    the mask holds the row and its ancestors."""
+    rng = np.random.default_rng(seed)
+    masks = []
+    for r in rows:
+        anc = []
+        for i in range(r):
+            par = int(rng.integers(-1, i)) if i else -1
+            m = (1 << i) | (anc[par] if par >= 0 else 0)
+            anc.append(m)
+            masks.append(m)
+    return masks
+
+
+def check_brute_tree(ora):
+    x = make_decode(2, 4, 2, rows=[4, 3], kv_lens=[7, 5], Lcap=8, seed=31)
+    Q, Kc, Vc, G = (f64(t) for t in (x.q, x.k_cache, x.v_cache, x.g))
+    masks = _tree_masks([4, 3], 5)
+    masks[1] = 0b10                                  # a row that does not see row 0
+    out, lse = ora.decode_tree(Q, Kc, Vc, G, x.kv_lens.tolist(), x.cu_rows.tolist(), masks)
+    ref = brute.decode_tree(Q, Kc, Vc, G, x.kv_lens.tolist(), [4, 3], masks)
+    for (t, h), (o, l) in ref.items():
+        e = _cmp(out[t, h], [float(v) for v in o], 1e-12, f"tree out {(t, h)}")
+        e = e or _cmp(lse[t, h], float(l), 1e-12, f"tree lse {(t, h)}")
+        if e:
+            return e
+    return ""
+
+
+def check_tree_chain_is_decode(ora):
+    """Chain masks (row i sees new rows 0..i) give the chain-verify result."""
+    y = make_decode(3, 8, 2, rows=[3, 1, 5], kv_lens=[9, 4, 12], Lcap=13, seed=32)
+    Q, Kc, Vc, G = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    a, al = ora.decode(Q, Kc, Vc, G, y.kv_lens.tolist(), y.cu_rows.tolist())
+    b, bl = ora.decode_tree(Q, Kc, Vc, G, y.kv_lens.tolist(), y.cu_rows.tolist(),
+                            ora.chain_masks([3, 1, 5]))
+    return _cmp(b, a, 1e-13, "chain tree") or _cmp(bl, al, 1e-13, "chain tree lse")
+
+
+def check_tree_storage_permutation(ora):
+    """Storing the new rows' keys in another order, with the mask bits renamed to
+    match, changes no output: only the visible set matters."""
+    r, L = 5, 11
+    y = make_decode(1, 4, 1, rows=[r], kv_lens=[L], Lcap=L, seed=33)
+    Q, Kc, Vc, G = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    masks = _tree_masks([r], 7)
+    a, _ = ora.decode_tree(Q, Kc, Vc, G, [L], [0, r], masks)
+    perm = [3, 0, 4, 1, 2]                           # new row k stored at slot perm[k]
+    base = L - r
+    K2, V2 = Kc.copy(), Vc.copy()
+    for k in range(r):
+        K2[0, :, base + perm[k]] = Kc[0, :, base + k]
+        V2[0, :, base + perm[k]] = Vc[0, :, base + k]
+    m2 = [sum(1 << perm[k] for k in range(r) if (m >> k) & 1) for m in masks]
+    b, _ = ora.decode_tree(Q, K2, V2, G, [L], [0, r], m2)
+    return _cmp(b, a, 1e-12, "tree permutation")
+
+
 CHECKS = [
     check_brute_prefill, check_brute_prefill_ungated, check_brute_decode, check_library_sdpa,
     check_one_key, check_gate_zero_half, check_gate_large_passthrough, check_equal_keys_mean,
     check_dominant_key, check_masked_keys_ignored, check_chunked_prefill,
     check_verify_equals_prefill, check_head_chunks, check_merge_partition,
-    check_merge_empty_row, check_plan_golden,
+    check_merge_empty_row, check_plan_golden, check_brute_tree, check_tree_chain_is_decode,
+    check_tree_storage_permutation,
 ]
 
 
