@@ -475,7 +475,41 @@ def ours(args):
             "split_kernel_gbs": round((v_kv + vx.q.numel() * 2) / (v_split / 1e3) / 1e9, 2),
             "split_plan": {"num_splits": vctx["plan"][0], "split_keys": vctx["plan"][1]},
             "ms_per_step": round(v_step, 5)}
-        del vctx, vx
+        # the same verify workload over seeded token trees (one 64-bit mask per row)
+        import gqa_head_gated_gb300 as G
+        tm = torch.tensor(S.random_tree_masks(vx.rows, 5), dtype=torch.int64, device=dev)
+        Bv, Hkvv = vx.k_cache.shape[:2]
+        Tv, Hqv = vx.q.shape[:2]
+        ws = torch.empty(G.decode_workspace_size(Bv, Tv, Hqv, Hkvv, max(vx.rows),
+                                                 vctx["max_kv"]), dtype=torch.uint8, device=dev)
+        tout = torch.empty_like(vctx["q"])
+        cud = vx.cu_rows.to(dev)
+
+        def tree_step():
+            G.verify_tree(vctx["q"], vctx["kc"], vctx["vc"], vctx["g"], vctx["kv"], cud, tm,
+                          max_rows=max(vx.rows), max_kv_len=vctx["max_kv"], workspace=ws,
+                          out=tout)
+        for _ in range(args.warmup):
+            vctx["flush"]()
+            tree_step()
+        torch.cuda.synchronize()
+        tms = []
+        for _ in range(args.steps):
+            vctx["flush"]()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record()
+            tree_step()
+            b_.record()
+            tms.append((a_, b_))
+        torch.cuda.synchronize()
+        t_avg = sum(a_.elapsed_time(b_) for a_, b_ in tms) / len(tms)
+        more["verify_tree_35b"] = {
+            "workload": "the 35B draft-verify workload over seeded token trees "
+                        "(synth.random_tree_masks(rows, 5)), gqa_attn_verify_tree",
+            "value": round(v_bytes / (t_avg / 1e3) / 1e9, 2), "unit": "GB/s",
+            "frac_of_hbm": round(v_bytes / (t_avg / 1e3) / 1e9 / hbm_peak, 4),
+            "ms_per_step": round(t_avg, 5)}
+        del vctx, vx, ws, tout
         torch.cuda.empty_cache()
 
     cpu = None

@@ -18,7 +18,7 @@ from ._lib import GqaError, check, load  # noqa: F401
 
 HEAD_DIM = 256
 
-__all__ = ["prefill", "decode", "decode_plan", "decode_split", "lse_merge",
+__all__ = ["prefill", "decode", "verify_tree", "decode_plan", "decode_split", "lse_merge",
            "decode_workspace_size", "last_device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "GqaError",
            "load"]
@@ -113,6 +113,38 @@ def decode(q, k_cache, v_cache, g, kv_lens, cu_rows=None, max_rows=None, max_kv_
                                   max_rows, max_kv_len, _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream())
     check(code, "gqa_attn_decode")
+    return (out, lse) if return_lse else out
+
+
+def verify_tree(q, k_cache, v_cache, g, kv_lens, cu_rows, tree_mask, max_rows=None,
+                max_kv_len=None, workspace=None, out=None, return_lse=False):
+    """Draft verify over token trees.  As decode(), plus tree_mask: int64 [T] CUDA
+    tensor, one mask per new row over its sequence's new rows (bit k: new row k
+    visible; its ancestors and itself).  Rows per sequence <= 64."""
+    _need(q, torch.bfloat16, 3, "q")
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    if g is not None:
+        _need(g, torch.bfloat16, 3, "g")
+    if cu_rows is None:
+        raise ValueError("cu_rows is required for tree verify")
+    if (tree_mask.dtype != torch.int64 or not tree_mask.is_cuda or not tree_mask.is_contiguous()
+            or tree_mask.numel() != q.shape[0]):
+        raise ValueError("tree_mask must be a contiguous int64 CUDA tensor of T entries")
+    T, Hq, B, Hkv, Lcap, max_rows, max_kv_len = _decode_sizes(q, k_cache, kv_lens, cu_rows,
+                                                               max_rows, max_kv_len)
+    need = decode_workspace_size(B, T, Hq, Hkv, max_rows, max_kv_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if return_lse else None
+    code = load().gqa_attn_verify_tree(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(g),
+                                       _ptr(kv_lens), _ptr(cu_rows), _ptr(tree_mask), _ptr(out),
+                                       _ptr(lse), B, T, Hq, Hkv, Lcap, max_rows, max_kv_len,
+                                       _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream())
+    check(code, "gqa_attn_verify_tree")
     return (out, lse) if return_lse else out
 
 

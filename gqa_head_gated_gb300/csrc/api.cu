@@ -130,11 +130,13 @@ size_t workspace_bytes_for(int T, int Hq, int S) {
 
 int run_split(const void* Q, const void* Kc, const void* Vc, const int* kv_lens,
               const int* cu_rows, float* O_parts, float* lse_parts, int B, int T, int Hq, int Hkv,
-              int Lcap, int max_rows, int max_kv_len, int S, int C, cudaStream_t stream) {
+              int Lcap, int max_rows, int max_kv_len, int S, int C, cudaStream_t stream,
+              const unsigned long long* tree_mask = nullptr) {
   LaunchCtl ctl;
   if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
   DecodeSplitArgs a{Q, Kc, Vc, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
                     max_rows, max_kv_len, S, C};
+  a.tree_mask = tree_mask;
   if (tc_path(Hq, Hkv, max_rows) && C % tc_split_keys_multiple() == 0) {
     bool encode_failed = false;
     const cudaError_t e = launch_decode_split_tc(a, ctl, stream, &encode_failed);
@@ -286,6 +288,35 @@ int gqa_attn_decode(const void* Q, const void* Kcache, const void* Vcache, const
   float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
   int r = gqa_attn_decode_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq,
                                 Hkv, Lcap, max_rows, max_kv_len, S, C, stream);
+  if (r != GQA_OK) return r;
+  return attn_lse_merge(O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
+}
+
+int gqa_attn_verify_tree(const void* Q, const void* Kcache, const void* Vcache, const void* G,
+                         const int* kv_lens, const int* cu_rows,
+                         const unsigned long long* tree_mask, void* out, float* lse_out, int B,
+                         int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                         void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
+  if (st != GQA_OK) return st;
+  if (max_rows > 64) return GQA_ERR_UNSUPPORTED;   // one 64-bit mask per row
+  if (T == 0) return GQA_OK;
+  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
+      cu_rows == nullptr || tree_mask == nullptr || out == nullptr)
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(out, 16) ||
+      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)) ||
+      !aligned(kv_lens, 4) || !aligned(cu_rows, 4) || !aligned(tree_mask, 8))
+    return GQA_ERR_INVALID_ARG;
+  int S = 0, C = 0;
+  plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
+  const size_t need = workspace_bytes_for(T, Hq, S);
+  if (workspace == nullptr || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return GQA_ERR_INVALID_ARG;
+  float* O_parts = static_cast<float*>(workspace);
+  float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
+  int r = run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
+                    max_rows, max_kv_len, S, C, static_cast<cudaStream_t>(stream), tree_mask);
   if (r != GQA_OK) return r;
   return attn_lse_merge(O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
 }

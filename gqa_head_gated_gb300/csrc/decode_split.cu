@@ -35,6 +35,7 @@ struct Params {
   const __nv_bfloat16* V;
   const int* kv_lens;
   const int* cu_rows;
+  const unsigned long long* tree_mask;   // null: chain verify
   float* O_parts;
   float* lse_parts;
   int B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, gqa, split_keys, num_splits, n_rb;
@@ -109,6 +110,7 @@ decode_split_kernel(const Params p) {
   __shared__ float s_m[WK][MB];
   __shared__ float s_l[WK][MB];
   __shared__ int s_lim[MB];
+  __shared__ unsigned long long s_mask[MB];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -138,16 +140,25 @@ decode_split_kernel(const Params p) {
   const int k_hi = min(k_lo + p.split_keys, kv_len);
 
   // Visible keys of each packed row of the block (0 for padding rows).
+  // Chain: row i sees keys < kv_len - rows + i + 1.  Tree: keys before the new rows,
+  // and new key base + k when bit k of the row's mask is set.
+  const bool tree = p.tree_mask != nullptr;
+  const int base = kv_len - rows;
   if (tid < MB) {
     const int pp = p0 + tid;
     int lim = 0;
-    if (pp < P) lim = kv_len - rows + pp / p.gqa + 1;
+    unsigned long long m = 0;
+    if (pp < P) {
+      lim = tree ? kv_len : base + pp / p.gqa + 1;
+      if (tree) m = p.tree_mask[t0 + pp / p.gqa];
+    }
     s_lim[tid] = min(lim, k_hi);
+    s_mask[tid] = m;
   }
   int n_hi = 0;   // keys any row of the block sees in this split
   {
     const int pl = min(P - 1, p0 + MB - 1);
-    n_hi = min(kv_len - rows + pl / p.gqa + 1, k_hi);
+    n_hi = min(tree ? kv_len : base + pl / p.gqa + 1, k_hi);
   }
   const int n_tiles = n_hi > k_lo ? (n_hi - k_lo + kTK - 1) / kTK : 0;
 
@@ -257,6 +268,7 @@ decode_split_kernel(const Params p) {
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int lim = s_lim[wr * 16 + g4 + 8 * hr];
+      const unsigned long long msk = s_mask[wr * 16 + g4 + 8 * hr];
       float mx = -INFINITY;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -264,7 +276,8 @@ decode_split_kernel(const Params p) {
         for (int e = 0; e < 2; ++e) {
           const int key = key_w + nt * 8 + 2 * t4 + e;
           float v = sc[nt][2 * hr + e];
-          v = key < lim ? v * kScaleLog2 : -INFINITY;
+          const bool vis = key < lim && (!tree || key < base || ((msk >> (key - base)) & 1ull));
+          v = vis ? v * kScaleLog2 : -INFINITY;
           sc[nt][2 * hr + e] = v;
           mx = fmaxf(mx, v);
         }
@@ -397,6 +410,7 @@ cudaError_t launch_decode_split(const DecodeSplitArgs& a, const LaunchCtl& ctl,
   p.V = static_cast<const __nv_bfloat16*>(a.V);
   p.kv_lens = a.kv_lens;
   p.cu_rows = a.cu_rows;
+  p.tree_mask = a.tree_mask;
   p.O_parts = a.O_parts;
   p.lse_parts = a.lse_parts;
   p.B = a.B;

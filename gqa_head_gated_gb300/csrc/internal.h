@@ -36,6 +36,9 @@ struct DecodeSplitArgs {
   float* O_parts;
   float* lse_parts;
   int B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, num_splits, split_keys;
+  // Tree verify: per new row, a mask over its sequence's new rows (bit k = new row
+  // k visible); null for chain verify / decode.
+  const unsigned long long* tree_mask = nullptr;
 };
 
 // Packed query rows (heads x rows of one KV group) per decode CTA: 16, 32 or 64.

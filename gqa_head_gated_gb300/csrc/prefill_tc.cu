@@ -45,6 +45,7 @@
 // MMA.  The epilogue writes the normalised
 // partial O / l (fp32) and lse = m + ln l for attn_lse_merge, or lse = -inf for a
 // row that sees no key of the split.
+#include <climits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -113,6 +114,7 @@ struct Params {
   // split mode
   const int* kv_lens;
   const int* cu_rows;
+  const unsigned long long* tree_mask;   // split mode, tree verify; null: chain
   float* O_parts;
   float* lse_parts;
   int T, Lcap, max_rows, max_kv_len, split_keys, num_splits;
@@ -210,7 +212,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     rows_here = min(p.R, rows - r0);
     const int k_lo = s_idx * p.split_keys;
     k_hi = min(k_lo + p.split_keys, kv_len);
-    n_hi = min(k_hi, kv_len - rows + r0 + rows_here);   // keys the tile's last row sees
+    // keys the tile's last row sees (a tree row may see up to the last new key)
+    n_hi = min(k_hi, p.tree_mask ? kv_len : kv_len - rows + r0 + rows_here);
     if (n_hi <= k_lo) {
       // No row of the tile sees a key of this split: empty parts.
       for (int m = threadIdx.x; m < rows_here * p.gqa; m += kThreads) {
@@ -414,8 +417,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       rr = row / p.gqa;                   // row m: token r0 + m / GQA, head m % GQA
       hh = row - rr * p.gqa;
       valid = (row < p.R * p.gqa) && (rr < rows_here);
-      lim = valid ? min(kv_len - rows + r0 + rr + 1, k_hi) : n_hi;
+      lim = valid ? min(p.tree_mask ? kv_len : kv_len - rows + r0 + rr + 1, k_hi) : n_hi;
     }
+    // Tree verify: new key kv_len - rows + k is visible only when bit k is set.
+    const unsigned long long tmask =
+        (kSplit && p.tree_mask != nullptr && valid) ? p.tree_mask[t0 + r0 + rr] : ~0ull;
+    const int tbase = kSplit && p.tree_mask != nullptr ? kv_len - rows : INT_MAX;
     const int q = r0 + rr;
     const uint32_t trow = tmem + (uint32_t(lq * 32) << 16);
 
@@ -441,6 +448,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
           for (int c = 0; c < kHalf; ++c)
             if (key0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
+        }
+        if (key0 + kHalf > tbase) {
+#pragma unroll
+          for (int c = 0; c < kHalf; ++c) {
+            const int k = key0 + c - tbase;
+            if (k >= 0 && k < 64 && !((tmask >> k) & 1ull)) s[c] = __float_as_uint(-INFINITY);
+          }
         }
         float m8[8];
 #pragma unroll
@@ -722,6 +736,7 @@ cudaError_t launch_decode_split_tc(const DecodeSplitArgs& a, const LaunchCtl& ct
   p.n_rtiles = (a.max_rows + R - 1) / R;
   p.kv_lens = a.kv_lens;
   p.cu_rows = a.cu_rows;
+  p.tree_mask = a.tree_mask;
   p.O_parts = a.O_parts;
   p.lse_parts = a.lse_parts;
   p.T = a.T;

@@ -113,6 +113,23 @@ int gqa_attn_decode(const void* Q, const void* Kcache, const void* Vcache, const
                     void* workspace, size_t workspace_bytes, gqa_stream_t stream);
 
 /*
+ * Draft verify over a token tree (TensorFold PR #1009, "Receipt": decode shapes
+ * plan chains and trees).  As gqa_attn_decode, except that new row i of a sequence
+ * sees every key before the sequence's new rows (positions < kv_lens[b] - r_b) and
+ * the new key at position kv_lens[b] - r_b + k exactly when bit k of
+ * tree_mask[t] is set (its ancestors and itself; a chain is bits 0..i).
+ * tree_mask: uint64 [T] (device, 8-byte aligned), one mask per new row.
+ * cu_rows is required; max_rows <= 64 (GQA_ERR_UNSUPPORTED above).  Same workspace
+ * size and split plan as gqa_attn_decode.  A row whose mask selects no key and that
+ * has no earlier key outputs zeros.
+ */
+int gqa_attn_verify_tree(const void* Q, const void* Kcache, const void* Vcache, const void* G,
+                         const int* kv_lens, const int* cu_rows,
+                         const unsigned long long* tree_mask, void* out, float* lse_out, int B,
+                         int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                         void* workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+/*
  * The split plan gqa_attn_decode uses: the number of key splits S and the keys
  * per split (a multiple of 64).  Split s of sequence b covers keys
  * [s*split_keys, min((s+1)*split_keys, kv_lens[b])).  Host-only; returns

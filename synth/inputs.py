@@ -133,6 +133,21 @@ def make_decode(B, Hq, Hkv, rows, kv_lens, Lcap=None, seed=0, pad_value=float("n
                         torch.tensor(cu, dtype=torch.int32), seed)
 
 
+def random_tree_masks(rows, seed):
+    """Seeded token trees for draft verify: new row i of each sequence takes a
+    uniformly drawn earlier row as parent, or none; its mask holds its own bit and
+    its ancestors' bits (bit k = new row k).  Returns a list of ints, one per row."""
+    gen = torch.Generator().manual_seed(seed)
+    out = []
+    for r in rows:
+        anc = []
+        for i in range(int(r)):
+            par = int(torch.randint(-1, i, (1,), generator=gen)) if i else -1
+            anc.append((1 << i) | (anc[par] if par >= 0 else 0))
+        out.extend(anc)
+    return out
+
+
 # ---------------------------------------------------------------------------
 # The five named workloads.
 # ---------------------------------------------------------------------------

@@ -142,3 +142,20 @@ def test_binding_refuses_cpu_tensors():
         G.prefill(q, q[:, :1], q[:, :1], q)
     with pytest.raises(TypeError):
         G.prefill(q.float(), q, q, q)
+
+
+def test_verify_tree_rejects_before_launch(lib):
+    f = lib.gqa_attn_verify_tree
+    base = dict(Q=16, K=32, V=48, G=None, kv=80, cu=96, tm=112, out=128, lse=None, B=2, T=4,
+                Hq=4, Hkv=2, Lcap=100, max_rows=2, max_kv=100, ws=144, wsb=1 << 30)
+    def call(**kw):
+        a = dict(base); a.update(kw)
+        return f(P(a["Q"]), P(a["K"]), P(a["V"]), P(a["G"]), P(a["kv"]), P(a["cu"]), P(a["tm"]),
+                 P(a["out"]), P(a["lse"]), a["B"], a["T"], a["Hq"], a["Hkv"], a["Lcap"],
+                 a["max_rows"], a["max_kv"], P(a["ws"]), a["wsb"], None)
+    assert call(max_rows=65, T=4) == 2          # more than 64 new rows: no 64-bit mask
+    assert call(tm=None) == 1
+    assert call(cu=None) == 1
+    assert call(tm=116) == 1                    # mask array not 8-byte aligned
+    assert call(wsb=8) == 5
+    assert call(T=0) == 0
