@@ -241,6 +241,39 @@ def decode_tree(Q, Kc, Vc, G, kv_lens, cu_rows, tree_masks, rows=None):
     return out, lse
 
 
+def kv_append(Kc, Vc, Knew, Vnew, kv_lens, cu_rows):
+    """Writes the new rows of each sequence into its cache after the keys it holds:
+    cache[b, g, kv_lens[b] + i] = new[cu_rows[b] + i, g] for i < rows of b.
+    Knew, Vnew: [T, Hkv, D] token-major; caches [B, Hkv, Lcap, D].  Returns new
+    arrays (the inputs are not modified).  This is the append the TensorFold
+    attention contract compares bit for bit (its control: an append one row late)."""
+    Kc, Vc = np.array(Kc, copy=True), np.array(Vc, copy=True)
+    cu = [int(x) for x in cu_rows]
+    for b in range(len(cu) - 1):
+        L = int(kv_lens[b])
+        r = cu[b + 1] - cu[b]
+        Kc[b, :, L:L + r] = np.swapaxes(np.asarray(Knew)[cu[b]:cu[b + 1]], 0, 1)
+        Vc[b, :, L:L + r] = np.swapaxes(np.asarray(Vnew)[cu[b]:cu[b + 1]], 0, 1)
+    return Kc, Vc
+
+
+def kv_keep(Kc, Vc, kv_lens, cu_rows, keep):
+    """After verifying r_b draft rows held at positions kv_lens[b] - r_b ..
+    kv_lens[b] - 1, keeps the accepted ones: draft row keep[b][k] moves to position
+    kv_lens[b] - r_b + k, in order.  Returns (new caches, new kv_lens)."""
+    Kc, Vc = np.array(Kc, copy=True), np.array(Vc, copy=True)
+    cu = [int(x) for x in cu_rows]
+    new_lens = []
+    for b in range(len(cu) - 1):
+        r = cu[b + 1] - cu[b]
+        base = int(kv_lens[b]) - r
+        src = [base + int(i) for i in keep[b]]
+        Kc[b, :, base:base + len(src)] = Kc[b][:, src]
+        Vc[b, :, base:base + len(src)] = Vc[b][:, src]
+        new_lens.append(base + len(src))
+    return Kc, Vc, new_lens
+
+
 def chain_masks(rows_per_seq):
     """Masks of chain verify: new row i sees new rows 0..i."""
     return [(1 << (i + 1)) - 1 for r in rows_per_seq for i in range(r)]

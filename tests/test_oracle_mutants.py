@@ -37,6 +37,9 @@ MUTANTS = {
     "tree: mask bits shifted": ("if (int(mask) >> k) & 1]", "if (int(mask) >> (k + 1)) & 1]"),
     "tree: self bit ignored": ("for k in range(rows) if (int(mask) >> k) & 1]",
                                "for k in range(rows) if (int(mask) >> k) & 1 and k != i]"),
+    "append one row late": ("        L = int(kv_lens[b])\n        r = cu[b + 1] - cu[b]\n        Kc[b, :, L:L + r]",
+                            "        L = int(kv_lens[b]) + 1\n        r = cu[b + 1] - cu[b]\n        Kc[b, :, L:L + r]"),
+    "keep from the wrong base": ("        base = int(kv_lens[b]) - r\n        src", "        base = int(kv_lens[b]) - r + 1\n        src"),
     "plan chunk one head too wide": ("c = min(gqa, limit // rows)", "c = min(gqa, limit // rows + 1)"),
     "plan ignores the row bound": ("rows > limit or ", ""),
 }

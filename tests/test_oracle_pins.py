@@ -349,13 +349,79 @@ def check_tree_storage_permutation(ora):
     return _cmp(b, a, 1e-12, "tree permutation")
 
 
+def check_kv_append_brute(ora):
+    """Append against an element-by-element loop; rows already in the cache, other
+    sequences and positions past the new rows are untouched."""
+    rng = np.random.default_rng(41)
+    B, Hkv, Lcap, D = 3, 2, 12, 256
+    Kc = rng.standard_normal((B, Hkv, Lcap, D))
+    Vc = rng.standard_normal((B, Hkv, Lcap, D))
+    rows, lens = [2, 0, 3], [4, 7, 9]
+    cu = [0, 2, 2, 5]
+    Kn = rng.standard_normal((5, Hkv, D))
+    Vn = rng.standard_normal((5, Hkv, D))
+    K2, V2 = ora.kv_append(Kc, Vc, Kn, Vn, lens, cu)
+    for b in range(B):
+        for g in range(Hkv):
+            for pos in range(Lcap):
+                i = pos - lens[b]
+                if 0 <= i < rows[b]:
+                    wk, wv = Kn[cu[b] + i, g], Vn[cu[b] + i, g]
+                else:
+                    wk, wv = Kc[b, g, pos], Vc[b, g, pos]
+                if not (np.array_equal(K2[b, g, pos], wk) and np.array_equal(V2[b, g, pos], wv)):
+                    return f"append wrong at {(b, g, pos)}"
+    return ""
+
+
+def check_kv_keep_brute(ora):
+    """Keep against an element-by-element loop, including keeping every row (no
+    change), keeping none, and a kept set whose destinations overlap its sources."""
+    rng = np.random.default_rng(42)
+    B, Hkv, Lcap, D = 3, 2, 16, 256
+    Kc = rng.standard_normal((B, Hkv, Lcap, D))
+    Vc = rng.standard_normal((B, Hkv, Lcap, D))
+    lens, cu = [10, 6, 15], [0, 5, 6, 12]
+    keep = [[1, 2, 4], [], [0, 1, 2, 3, 4, 5]]
+    K2, V2, nl = ora.kv_keep(Kc, Vc, lens, cu, keep)
+    for b in range(B):
+        r = cu[b + 1] - cu[b]
+        base = lens[b] - r
+        if nl[b] != base + len(keep[b]):
+            return "kept length"
+        for g in range(Hkv):
+            for pos in range(Lcap):
+                k = pos - base
+                src = base + keep[b][k] if 0 <= k < len(keep[b]) else pos
+                if not (np.array_equal(K2[b, g, pos], Kc[b, g, src]) and
+                        np.array_equal(V2[b, g, pos], Vc[b, g, src])):
+                    return f"keep wrong at {(b, g, pos)}"
+    return ""
+
+
+def check_append_then_chain_verify(ora):
+    """Appending the new rows' K/V and running chain verify equals attending over the
+    old keys plus the new rows' own keys: the append lands where verify reads."""
+    y = make_decode(1, 4, 2, rows=[3], kv_lens=[8], Lcap=8, seed=43)
+    Q, Kc, Vc, G = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    Kn, Vn = Kc[0, :, 5:8].swapaxes(0, 1).copy(), Vc[0, :, 5:8].swapaxes(0, 1).copy()
+    blank_k, blank_v = Kc.copy(), Vc.copy()
+    blank_k[:, :, 5:] = 0.0
+    blank_v[:, :, 5:] = 0.0
+    K2, V2 = ora.kv_append(blank_k, blank_v, Kn, Vn, [5], [0, 3])
+    a, _ = ora.decode(Q, K2, V2, G, [8], [0, 3])
+    b, _ = ora.decode(Q, Kc, Vc, G, [8], [0, 3])
+    return "" if np.array_equal(a, b) else "append then verify differs"
+
+
 CHECKS = [
     check_brute_prefill, check_brute_prefill_ungated, check_brute_decode, check_library_sdpa,
     check_one_key, check_gate_zero_half, check_gate_large_passthrough, check_equal_keys_mean,
     check_dominant_key, check_masked_keys_ignored, check_chunked_prefill,
     check_verify_equals_prefill, check_head_chunks, check_merge_partition,
     check_merge_empty_row, check_plan_golden, check_brute_tree, check_tree_chain_is_decode,
-    check_tree_storage_permutation,
+    check_tree_storage_permutation, check_kv_append_brute, check_kv_keep_brute,
+    check_append_then_chain_verify,
 ]
 
 
