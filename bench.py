@@ -511,6 +511,34 @@ def ours(args):
             "ms_per_step": round(t_avg, 5)}
         del vctx, vx, ws, tout
         torch.cuda.empty_cache()
+        # KV-cache append of a whole 8192-row prompt's K/V (24/4 heads) into a cache
+        kn = pf.k.to(dev)[0].transpose(0, 1).contiguous()      # [8192, 4, 256]
+        vn = pf.v.to(dev)[0].transpose(0, 1).contiguous()
+        kcache = torch.empty((1, 4, 16384, 256), dtype=torch.bfloat16, device=dev)
+        vcache = torch.empty_like(kcache)
+        zl = torch.zeros(1, dtype=torch.int32, device=dev)
+        cu1 = torch.tensor([0, 8192], dtype=torch.int32, device=dev)
+        for _ in range(args.warmup):
+            G.kv_append(kn, vn, zl, kcache, vcache, cu1)
+        torch.cuda.synchronize()
+        aps = []
+        for _ in range(args.steps):
+            ctx["flush"]()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record()
+            G.kv_append(kn, vn, zl, kcache, vcache, cu1)
+            b_.record()
+            aps.append((a_, b_))
+        torch.cuda.synchronize()
+        ap_ms = sum(a_.elapsed_time(b_) for a_, b_ in aps) / len(aps)
+        ap_bytes = 2 * 2 * kn.numel() * 2                       # K and V, read and written
+        more["kv_append_27b_prompt"] = {
+            "workload": "gqa_kv_append of 8192 new rows x 4 KV heads (K and V, 33.5 MB) into "
+                        "a [1,4,16384,256] cache",
+            "value": round(ap_bytes / (ap_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "frac_of_hbm": round(ap_bytes / (ap_ms / 1e3) / 1e9 / hbm_peak, 4),
+            "ms_per_call": round(ap_ms, 5)}
+        del kn, vn, kcache, vcache
 
     cpu = None
     if rank == 0:

@@ -18,7 +18,7 @@ from ._lib import GqaError, check, load  # noqa: F401
 
 HEAD_DIM = 256
 
-__all__ = ["prefill", "decode", "verify_tree", "decode_plan", "decode_split", "lse_merge",
+__all__ = ["prefill", "decode", "verify_tree", "kv_append", "kv_keep", "decode_plan", "decode_split", "lse_merge",
            "decode_workspace_size", "last_device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "GqaError",
            "load"]
@@ -146,6 +146,32 @@ def verify_tree(q, k_cache, v_cache, g, kv_lens, cu_rows, tree_mask, max_rows=No
                                        workspace.numel() * workspace.element_size(), _stream())
     check(code, "gqa_attn_verify_tree")
     return (out, lse) if return_lse else out
+
+
+def kv_append(k_new, v_new, kv_lens, k_cache, v_cache, cu_rows=None):
+    """Writes new rows ([T,Hkv,256] bf16) after the kv_lens[b] keys each sequence
+    holds in the caches ([B,Hkv,Lcap,256]); kv_lens itself is not updated."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, 3, n)
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    T, Hkv, _ = k_new.shape
+    B, _, Lcap, _ = k_cache.shape
+    check(load().gqa_kv_append(_ptr(k_new), _ptr(v_new), _ptr(cu_rows), _ptr(kv_lens),
+                               _ptr(k_cache), _ptr(v_cache), B, T, Hkv, Lcap, _stream()),
+          "gqa_kv_append")
+
+
+def kv_keep(k_cache, v_cache, kv_lens, cu_rows, keep_idx, cu_keep, kv_lens_out=None):
+    """Moves the accepted draft rows (keep_idx, per sequence via cu_keep, strictly
+    increasing draft-row indices) to the front of each sequence's draft region, in
+    place; writes the new lengths into kv_lens_out when given."""
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    B, Hkv, Lcap, _ = k_cache.shape
+    check(load().gqa_kv_keep(_ptr(k_cache), _ptr(v_cache), _ptr(kv_lens), _ptr(cu_rows),
+                             _ptr(keep_idx), _ptr(cu_keep), _ptr(kv_lens_out), B, Hkv, Lcap,
+                             _stream()), "gqa_kv_keep")
 
 
 def decode_split(q, k_cache, v_cache, kv_lens, cu_rows=None, max_rows=None, max_kv_len=None,

@@ -40,6 +40,8 @@ SIGNATURES = {
     "gqa_last_device_status": (_I, [_P]),
     "gqa_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "gqa_selftest_wait_timeout": (_I, [_P, _P]),
+    "gqa_kv_append": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "gqa_kv_keep": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "gqa_attn_verify_tree": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                   _P, ctypes.c_size_t, _P]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,

@@ -213,6 +213,35 @@ int gqa_last_device_status(gqa_stream_t stream);
 void gqa_set_wait_timeout_ns(unsigned long long ns);
 
 /*
+ * KV-cache append (TensorFold PR #1009, "Receipt": packing, append and keep are
+ * compared bit for bit).  Writes the new K and V rows of each sequence after the
+ * keys it holds: Kcache[b, g, kv_lens[b] + i, :] = Knew[cu_rows[b] + i, g, :]
+ * (likewise V), i < rows of b.  This is also the layout change ("pack") from the
+ * token-major projection output to the head-major cache.
+ * Knew, Vnew: bf16 [T, Hkv, 256] (device); Kcache, Vcache: [B, Hkv, Lcap, 256];
+ * kv_lens: int32 [B] (device), keys held before the append (not updated here);
+ * cu_rows: int32 [B+1] (device) or NULL for one row per sequence (T == B).
+ * A row that would land at or past Lcap is skipped and GQA_ERR_DEVICE_RANGE is
+ * recorded.  Bit-exact copies.
+ */
+int gqa_kv_append(const void* Knew, const void* Vnew, const int* cu_rows, const int* kv_lens,
+                  void* Kcache, void* Vcache, int B, int T, int Hkv, int Lcap,
+                  gqa_stream_t stream);
+
+/*
+ * KV-cache keep after draft verification.  Sequence b holds r_b = cu_rows[b+1] -
+ * cu_rows[b] draft rows at positions kv_lens[b] - r_b .. kv_lens[b] - 1; the
+ * accepted ones, keep_idx[cu_keep[b] .. cu_keep[b+1]) (draft-row indices, strictly
+ * increasing), move in order to positions kv_lens[b] - r_b + k, in place.
+ * kv_lens_out: NULL or int32 [B] (device, must not alias kv_lens) receiving
+ * kv_lens[b] - r_b + (number kept).  A sequence with an invalid keep list is left
+ * untouched and GQA_ERR_DEVICE_RANGE is recorded.  Bit-exact copies.
+ */
+int gqa_kv_keep(void* Kcache, void* Vcache, const int* kv_lens, const int* cu_rows,
+                const int* keep_idx, const int* cu_keep, int* kv_lens_out, int B, int Hkv,
+                int Lcap, gqa_stream_t stream);
+
+/*
  * Failure-detection self test.  Launches one warp that runs the kernels' bounded
  * spin wait (the same code every mbarrier wait in the kernels uses) on a barrier
  * that nothing completes.  After the bound (gqa_set_wait_timeout_ns) it records

@@ -159,3 +159,15 @@ def test_verify_tree_rejects_before_launch(lib):
     assert call(tm=116) == 1                    # mask array not 8-byte aligned
     assert call(wsb=8) == 5
     assert call(T=0) == 0
+
+
+def test_kv_append_keep_reject_before_launch(lib):
+    a = lib.gqa_kv_append
+    assert a(P(16), P(32), None, P(48), P(64), P(80), 2, 3, 2, 10, None) == 1   # T != B without cu_rows
+    assert a(P(16), P(32), P(96), P(48), P(64), P(80), 0, 3, 2, 10, None) == 1
+    assert a(P(8), P(32), P(96), P(48), P(64), P(80), 2, 3, 2, 10, None) == 1    # misaligned
+    assert a(P(16), P(32), P(96), P(48), P(64), P(80), 2, 0, 2, 10, None) == 0
+    k = lib.gqa_kv_keep
+    assert k(P(16), P(32), P(48), P(64), P(80), P(96), P(48), 2, 2, 10, None) == 1  # out aliases in
+    assert k(P(16), P(32), P(48), None, P(80), P(96), None, 2, 2, 10, None) == 1
+    assert k(P(16), P(32), P(48), P(64), P(80), P(96), None, 0, 2, 10, None) == 1
