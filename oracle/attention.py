@@ -285,8 +285,10 @@ def lse_merge(O_parts, lse_parts, G=None):
     O_parts [S,N,D]: each part normalised (sum_j p_j V_j / l_s over its keys);
     lse_parts [S,N]: m_s + ln l_s of the part, -inf for a part with no key.
     out_n = sum_s exp(lse_s) O_s / sum_s exp(lse_s), times sigmoid(G) when given;
-    lse_n = ln sum_s exp(lse_s).  Parts of weight 0 are not read.  A row whose
-    parts are all empty outputs zeros and lse -inf.
+    lse_n = ln sum_s exp(lse_s).  Parts of weight 0 (lse -inf) are not read.  A
+    row whose parts are all empty outputs zeros and lse -inf.  A NaN or +Inf lse
+    enters the sums as float64 arithmetic takes it (weight NaN: the row is NaN), so
+    a part that saw a NaN score poisons its row as it would in the unsplit row.
 
     This is the tail-chunk merge the TensorFold attention contract checks (its
     control "a merge dropping later tail chunks" must fail).
@@ -297,10 +299,10 @@ def lse_merge(O_parts, lse_parts, G=None):
     out = np.zeros((N, D))
     lse = np.full(N, -np.inf)
     for n in range(N):
-        live = [s for s in range(S) if np.isfinite(lse_parts[s, n])]
+        live = [s for s in range(S) if lse_parts[s, n] != -np.inf]
         if not live:
             continue
-        M = max(lse_parts[s, n] for s in live)
+        M = float(np.max(lse_parts[live, n]))          # NaN if any part is NaN
         w = np.array([math.exp(lse_parts[s, n] - M) for s in live])
         acc = np.zeros(D)
         for ws, s in zip(w, live):

@@ -28,8 +28,14 @@ MUTANTS = {
     "dropped max shift": ("m = np.where(live, s.max(axis=1), 0.0)", "m = np.where(live, 0.0 * s.max(axis=1), 0.0)"),
     "gate sign": ("return 1.0 / (1.0 + np.exp(-x))", "return 1.0 / (1.0 + np.exp(x))"),
     "lse without ln l": ("lse[live] = m[live] + np.log(l[live])", "lse[live] = m[live]"),
-    "merge drops last part": ("live = [s for s in range(S) if np.isfinite(lse_parts[s, n])]",
-                              "live = [s for s in range(S) if np.isfinite(lse_parts[s, n])][:-1]"),
+    "merge drops last part": ("live = [s for s in range(S) if lse_parts[s, n] != -np.inf]",
+                              "live = [s for s in range(S) if lse_parts[s, n] != -np.inf][:-1]"),
+    "merge skips NaN parts": ("live = [s for s in range(S) if lse_parts[s, n] != -np.inf]",
+                              "live = [s for s in range(S) if np.isfinite(lse_parts[s, n])]"),
+    "sigmoid clamps the gate": ("return 1.0 / (1.0 + np.exp(-x))",
+                                "return 1.0 / (1.0 + np.exp(-np.nan_to_num(x)))"),
+    "scores without NaN": ("s = np.where(seen, s, -np.inf)",
+                           "s = np.where(seen & ~np.isnan(s), s, -np.inf)"),
     "merge ignores weights": ("acc += ws * O_parts[s, n]", "acc += O_parts[s, n]"),
     "plan drops remainder": ("    if gqa % c:\n        plan.append(gqa % c)\n", ""),
     "tree: new rows start one key late": ("    base = kv_len - rows\n    return list(range(base))",

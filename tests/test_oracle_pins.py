@@ -11,7 +11,14 @@
   chunks equal the unchunked group, an LSE merge of any key partition equals the
   unsplit row;
 * the head-chunk plan against the worked example the DS4Server issue113 README
-  prints (tests/golden/head_chunk_plan.txt).
+  prints (tests/golden/head_chunk_plan.txt);
+* non-finite inputs (the TensorFold attention contract's gate 1 plants them and
+  compares with float64): what IEEE arithmetic of the formula fixes -- a NaN
+  query row is NaN, an Inf value under a positive probability is Inf in that
+  column only, an Inf score poisons exactly the rows whose score is +Inf and
+  drops the key where it is -Inf (checked by brute force over the other keys),
+  a -Inf gate gives 0, a NaN merge part gives a NaN row, and non-finite values
+  in positions no row sees change nothing.
 
 Each check is a function returning an error string (empty when it holds) so that
 test_oracle_mutants.py can run the same checks against oracles with planted
@@ -414,6 +421,141 @@ def check_append_then_chain_verify(ora):
     return "" if np.array_equal(a, b) else "append then verify differs"
 
 
+# ---------------------------------------------------------------------------
+# non-finite inputs
+# ---------------------------------------------------------------------------
+
+def _same_except(a, b, mask):
+    """a equals b bit for bit outside `mask` (a boolean array of a's shape)."""
+    return np.array_equal(np.where(mask, 0.0, a), np.where(mask, 0.0, b))
+
+
+def check_nonfinite_q_row(ora):
+    """A NaN query row gives NaN out and lse for that row; other rows unchanged."""
+    x = make_prefill(1, 4, 2, 6, Lkv=9, kv_offset=3, seed=40)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    a, la = ora.prefill(Q, K, V, G, 3)
+    Q[0, 1, 2, 7] = np.nan
+    b, lb = ora.prefill(Q, K, V, G, 3)
+    if not (np.isnan(b[0, 1, 2]).all() and np.isnan(lb[0, 1, 2])):
+        return "NaN query row is not NaN"
+    m = np.zeros(a.shape, bool)
+    m[0, 1, 2] = True
+    return "" if _same_except(b, a, m) else "NaN query row changed another row"
+
+
+def check_nonfinite_v_column(ora):
+    """+Inf and -Inf in two columns of a key every row sees: every row of the KV
+    group is +Inf / -Inf in exactly those columns (p > 0, gate > 0); NaN in a
+    third column is NaN there; other heads and columns are unchanged."""
+    x = make_prefill(1, 4, 2, 5, Lkv=8, kv_offset=3, seed=41)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    a, la = ora.prefill(Q, K, V, G, 3)
+    V[0, 1, 0, 10] = np.inf
+    V[0, 1, 2, 20] = -np.inf
+    V[0, 1, 1, 30] = np.nan
+    b, lb = ora.prefill(Q, K, V, G, 3)
+    grp = b[0, 2:4]                        # heads 2, 3 read KV head 1
+    if not (np.all(grp[..., 10] == np.inf) and np.all(grp[..., 20] == -np.inf)
+            and np.all(np.isnan(grp[..., 30]))):
+        return "Inf/NaN value column did not propagate"
+    m = np.zeros(a.shape, bool)
+    m[0, 2:4, :, [10, 20, 30]] = True
+    if not _same_except(b, a, m):
+        return "Inf value changed other columns"
+    return "" if np.array_equal(la, lb) else "Inf value changed lse"
+
+
+def check_nonfinite_k_sign(ora):
+    """K[key 0, d] = +Inf: rows whose q_d > 0 score +Inf (NaN row); rows with
+    q_d < 0 score -Inf on key 0, which drops out -- checked by brute force over
+    keys 1..lim."""
+    y = make_decode(1, 4, 2, rows=[3], kv_lens=[6], Lcap=8, seed=42, pad_value=0.0)
+    Q, Kc, Vc, G = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    d = 5
+    Kc[0, :, 0, d] = np.inf
+    out, lse = ora.decode(Q, Kc, Vc, G, [6], [0, 3])
+    seen_neg = 0
+    for t in range(3):
+        lim = 6 - 3 + t + 1
+        for h in range(4):
+            g = h // 2
+            if Q[t, h, d] > 0:
+                if not (np.isnan(out[t, h]).all() and np.isnan(lse[t, h])):
+                    return "+Inf score did not give a NaN row"
+            else:
+                seen_neg += 1
+                o, l = brute._row(Q[t, h], [Kc[0, g, j] for j in range(1, lim)],
+                                  [Vc[0, g, j] for j in range(1, lim)], G[t, h])
+                e = _cmp(out[t, h], [float(v) for v in o], 1e-13, "-Inf score drops key")
+                if e:
+                    return e
+    return "" if seen_neg else "no row with q_d < 0 (pick another seed)"
+
+
+def check_nonfinite_k_nan(ora):
+    """A NaN in key 1 makes every row that sees key 1 NaN (its score is NaN);
+    row 0 of a prompt from position 0 does not see it and is unchanged."""
+    x = make_prefill(1, 2, 1, 4, seed=46)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    a, _ = ora.prefill(Q, K, V, G, 0)
+    K[0, 0, 1, 100] = np.nan
+    b, lb = ora.prefill(Q, K, V, G, 0)
+    if not np.array_equal(a[:, :, 0], b[:, :, 0]):
+        return "NaN key changed a row that does not see it"
+    return "" if np.isnan(b[:, :, 1:]).all() and np.isnan(lb[:, :, 1:]).all() else "NaN key"
+
+
+def check_nonfinite_gate(ora):
+    """Gate -Inf gives exactly 0, +Inf passes the attention through, NaN is NaN."""
+    x = make_prefill(1, 2, 1, 3, seed=43)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    plain, _ = ora.prefill(Q, K, V, None, 0)
+    G[0, 0, 1, 3] = -np.inf
+    G[0, 0, 1, 4] = np.inf
+    G[0, 1, 2, 5] = np.nan
+    out, _ = ora.prefill(Q, K, V, G, 0)
+    if out[0, 0, 1, 3] != 0.0 or out[0, 0, 1, 4] != plain[0, 0, 1, 4]:
+        return "infinite gate"
+    return "" if np.isnan(out[0, 1, 2, 5]) else "NaN gate"
+
+
+def check_nonfinite_unseen(ora):
+    """NaN/Inf in K and V positions no row sees (prompt keys past the last row,
+    cache rows past kv_len) and in K of keys masked for a row change nothing in
+    the rows that do not see them."""
+    x = make_prefill(1, 4, 2, 6, Lkv=12, kv_offset=2, seed=44)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    a, _ = ora.prefill(Q, K, V, G, 2)
+    K[:, :, 8:] = np.nan                  # positions 8..11: past the last row (7)
+    V[:, :, 8:] = -np.inf
+    K[:, 0, 6, 0] = np.inf                # key 6: rows 4, 5 see it
+    b, _ = ora.prefill(Q, K, V, G, 2)
+    if not np.array_equal(a[:, :, :4], b[:, :, :4]) or not np.array_equal(a[:, 2:], b[:, 2:]):
+        return "unseen non-finite keys changed a row"
+    y = make_decode(2, 4, 2, rows=[2, 1], kv_lens=[5, 3], Lcap=9, seed=45, pad_value=np.inf)
+    Qd, Kd, Vd, Gd = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    c, _ = ora.decode(Qd, Kd, Vd, Gd, [5, 3], y.cu_rows.tolist())
+    Kd[0, :, 5:] = np.nan
+    Vd[1, :, 3:] = -np.inf
+    e, _ = ora.decode(Qd, Kd, Vd, Gd, [5, 3], y.cu_rows.tolist())
+    return "" if np.array_equal(c, e) and np.isfinite(c).all() else "cache padding changed a row"
+
+
+def check_nonfinite_merge(ora):
+    """A NaN part makes its row NaN (out and lse); a -inf part with NaN O is not
+    read; +Inf lse gives NaN (exp(Inf - Inf))."""
+    parts = np.ones((3, 3, 256))
+    lses = np.array([[0.1, 0.2, 0.3], [np.nan, -np.inf, np.inf], [0.5, 0.5, 0.5]])
+    parts[1, 1] = np.nan
+    out, lse = ora.lse_merge(parts, lses)
+    if not (np.isnan(out[0]).all() and np.isnan(lse[0])):
+        return "NaN part did not poison its row"
+    if not (np.all(out[1] == 1.0) and np.isfinite(lse[1])):
+        return "-inf part was read"
+    return "" if np.isnan(out[2]).all() and np.isnan(lse[2]) else "+Inf lse"
+
+
 CHECKS = [
     check_brute_prefill, check_brute_prefill_ungated, check_brute_decode, check_library_sdpa,
     check_one_key, check_gate_zero_half, check_gate_large_passthrough, check_equal_keys_mean,
@@ -421,7 +563,8 @@ CHECKS = [
     check_verify_equals_prefill, check_head_chunks, check_merge_partition,
     check_merge_empty_row, check_plan_golden, check_brute_tree, check_tree_chain_is_decode,
     check_tree_storage_permutation, check_kv_append_brute, check_kv_keep_brute,
-    check_append_then_chain_verify,
+    check_append_then_chain_verify, check_nonfinite_q_row, check_nonfinite_v_column,
+    check_nonfinite_k_sign, check_nonfinite_k_nan, check_nonfinite_gate, check_nonfinite_unseen, check_nonfinite_merge,
 ]
 
 
