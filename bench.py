@@ -539,6 +539,37 @@ def ours(args):
             "frac_of_hbm": round(ap_bytes / (ap_ms / 1e3) / 1e9 / hbm_peak, 4),
             "ms_per_call": round(ap_ms, 5)}
         del kn, vn, kcache, vcache
+        torch.cuda.empty_cache()
+        # FP16 twins of the headline decode and of the 27B prefill (same draws rounded to
+        # fp16, the _f16 entry points; same byte and FLOP counts as bf16)
+        xf = S.decode_27b(dtype=torch.float16)
+        fctx = setup_decode(xf, args.steps, dev)
+        run_decode_timed(fctx, args.warmup)
+        torch.cuda.synchronize()
+        run_decode_timed(fctx, args.steps)
+        torch.cuda.synchronize()
+        f_split = sum(a.elapsed_time(m) for a, m, b in fctx["ev"]) / args.steps
+        f_step = sum(a.elapsed_time(b) for a, m, b in fctx["ev"]) / args.steps
+        f_ok = bool(torch.isfinite(fctx["out"].float()).all().item())
+        more["decode_27b_fp16"] = {
+            "workload": "the 27B-shape decode workload in fp16 (gqa_attn_decode_split_f16 + "
+                        "attn_lse_merge_f16)",
+            "value": round(step_bytes / (f_step / 1e3) / 1e9, 2), "unit": "GB/s",
+            "frac_of_hbm": round(step_bytes / (f_step / 1e3) / 1e9 / hbm_peak, 4),
+            "split_kernel_gbs": round(split_bytes / (f_split / 1e3) / 1e9, 2),
+            "ms_per_step": round(f_step, 5), "outputs_finite": f_ok}
+        del fctx, xf
+        torch.cuda.empty_cache()
+        pff = S.prefill_27b(dtype=torch.float16)
+        pff_ms = bench_prefill(pff, pf_steps, max(3, args.warmup), dev, e2e=False)[0]
+        pff_avg = sum(pff_ms) / len(pff_ms)
+        more["prefill_27b_fp16"] = {
+            "workload": "the 27B-shape prefill in fp16 (gqa_attn_prefill_f16)",
+            "value": round(flops / (pff_avg / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+            "frac_of_fp16_peak": round(flops / (pff_avg / 1e3) / 1e12 / bf16_peak, 4),
+            "peak_note": "fp16 dense peak = measured bf16 burst peak x 1 (equal nominal rates)",
+            "avg_ms": round(pff_avg, 4)}
+        del pff
 
     cpu = None
     if rank == 0:

@@ -4,7 +4,8 @@ Thin PyTorch binding over the C ABI of libgqa_attn.so (include/gqa_attn.h).
 It only checks and marshals arguments (pointers, sizes, the current CUDA
 stream) and allocates outputs with torch; every step of the computation runs in
 the library's CUDA kernels.  There is no CPU fallback: without the shared
-library or a CUDA device the calls raise.
+library or a CUDA device the calls raise.  Every attention call takes bf16 or
+fp16 tensors (one type per call) and picks the matching entry point.
 
     out = softmax(Q K^T / 16 + causal/offset mask) V * sigmoid(G)
 """
@@ -32,6 +33,18 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_ELEM = {torch.bfloat16: "", torch.float16: "_f16"}
+
+
+def _elem(t, name):
+    """Entry-point suffix for the element type of `t` (bf16 or fp16)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in _ELEM:
+        raise TypeError(f"{name} must be bfloat16 or float16, got {t.dtype}")
+    return _ELEM[t.dtype]
+
+
 def _need(t, dtype, ndim, name):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -46,20 +59,24 @@ def _need(t, dtype, ndim, name):
 def prefill(q, k, v, g=None, kv_offset=0, out=None, return_lse=False):
     """Prompt rows.  q, g: [B,Hq,Lq,256] bf16; k, v: [B,Hkv,Lkv,256] bf16.
     Row i sits at position kv_offset + i and sees keys 0..kv_offset+i.
-    Returns out [B,Hq,Lq,256] bf16 (and lse [B,Hq,Lq] fp32 if return_lse)."""
-    _need(q, torch.bfloat16, 4, "q")
-    _need(k, torch.bfloat16, 4, "k")
-    _need(v, torch.bfloat16, 4, "v")
+    Returns out [B,Hq,Lq,256] bf16 (and lse [B,Hq,Lq] fp32 if return_lse).
+    fp16 inputs run the fp16 kernels and give an fp16 out."""
+    sfx = _elem(q, "q")
+    _need(q, q.dtype, 4, "q")
+    _need(k, q.dtype, 4, "k")
+    _need(v, q.dtype, 4, "v")
     if g is not None:
-        _need(g, torch.bfloat16, 4, "g")
+        _need(g, q.dtype, 4, "g")
     B, Hq, Lq, _ = q.shape
     Hkv, Lkv = k.shape[1], k.shape[2]
     if out is None:
         out = torch.empty_like(q)
     lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device) if return_lse else None
-    code = load().gqa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(lse),
-                                   B, Hq, Hkv, Lq, Lkv, int(kv_offset), _stream())
-    check(code, "gqa_attn_prefill")
+    _need(out, q.dtype, 4, "out")
+    fn = getattr(load(), "gqa_attn_prefill" + sfx)
+    code = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq, Lkv,
+              int(kv_offset), _stream())
+    check(code, "gqa_attn_prefill" + sfx)
     return (out, lse) if return_lse else out
 
 
@@ -94,12 +111,14 @@ def decode(q, k_cache, v_cache, g, kv_lens, cu_rows=None, max_rows=None, max_kv_
            workspace=None, out=None, return_lse=False):
     """Decode / chain-verify rows.  q, g: [T,Hq,256] bf16 token-major; caches
     [B,Hkv,Lcap,256] bf16; kv_lens int32 [B] (counts the new rows); cu_rows int32
-    [B+1] or None (one row per sequence).  Returns out [T,Hq,256] bf16."""
-    _need(q, torch.bfloat16, 3, "q")
-    _need(k_cache, torch.bfloat16, 4, "k_cache")
-    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    [B+1] or None (one row per sequence).  Returns out [T,Hq,256] bf16 (fp16 for
+    fp16 inputs)."""
+    sfx = _elem(q, "q")
+    _need(q, q.dtype, 3, "q")
+    _need(k_cache, q.dtype, 4, "k_cache")
+    _need(v_cache, q.dtype, 4, "v_cache")
     if g is not None:
-        _need(g, torch.bfloat16, 3, "g")
+        _need(g, q.dtype, 3, "g")
     T, Hq, B, Hkv, Lcap, max_rows, max_kv_len = _decode_sizes(q, k_cache, kv_lens, cu_rows,
                                                                max_rows, max_kv_len)
     need = decode_workspace_size(B, T, Hq, Hkv, max_rows, max_kv_len)
@@ -108,11 +127,12 @@ def decode(q, k_cache, v_cache, g, kv_lens, cu_rows=None, max_rows=None, max_kv_
     if out is None:
         out = torch.empty_like(q)
     lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if return_lse else None
-    code = load().gqa_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(g), _ptr(kv_lens),
-                                  _ptr(cu_rows), _ptr(out), _ptr(lse), B, T, Hq, Hkv, Lcap,
-                                  max_rows, max_kv_len, _ptr(workspace),
-                                  workspace.numel() * workspace.element_size(), _stream())
-    check(code, "gqa_attn_decode")
+    _need(out, q.dtype, 3, "out")
+    fn = getattr(load(), "gqa_attn_decode" + sfx)
+    code = fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(g), _ptr(kv_lens), _ptr(cu_rows),
+              _ptr(out), _ptr(lse), B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, _ptr(workspace),
+              workspace.numel() * workspace.element_size(), _stream())
+    check(code, "gqa_attn_decode" + sfx)
     return (out, lse) if return_lse else out
 
 
@@ -120,12 +140,13 @@ def verify_tree(q, k_cache, v_cache, g, kv_lens, cu_rows, tree_mask, max_rows=No
                 max_kv_len=None, workspace=None, out=None, return_lse=False):
     """Draft verify over token trees.  As decode(), plus tree_mask: int64 [T] CUDA
     tensor, one mask per new row over its sequence's new rows (bit k: new row k
-    visible; its ancestors and itself).  Rows per sequence <= 64."""
-    _need(q, torch.bfloat16, 3, "q")
-    _need(k_cache, torch.bfloat16, 4, "k_cache")
-    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    visible; its ancestors and itself).  Rows per sequence <= 64.  bf16 or fp16."""
+    sfx = _elem(q, "q")
+    _need(q, q.dtype, 3, "q")
+    _need(k_cache, q.dtype, 4, "k_cache")
+    _need(v_cache, q.dtype, 4, "v_cache")
     if g is not None:
-        _need(g, torch.bfloat16, 3, "g")
+        _need(g, q.dtype, 3, "g")
     if cu_rows is None:
         raise ValueError("cu_rows is required for tree verify")
     if (tree_mask.dtype != torch.int64 or not tree_mask.is_cuda or not tree_mask.is_contiguous()
@@ -139,22 +160,24 @@ def verify_tree(q, k_cache, v_cache, g, kv_lens, cu_rows, tree_mask, max_rows=No
     if out is None:
         out = torch.empty_like(q)
     lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if return_lse else None
-    code = load().gqa_attn_verify_tree(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(g),
-                                       _ptr(kv_lens), _ptr(cu_rows), _ptr(tree_mask), _ptr(out),
-                                       _ptr(lse), B, T, Hq, Hkv, Lcap, max_rows, max_kv_len,
-                                       _ptr(workspace),
-                                       workspace.numel() * workspace.element_size(), _stream())
-    check(code, "gqa_attn_verify_tree")
+    _need(out, q.dtype, 3, "out")
+    fn = getattr(load(), "gqa_attn_verify_tree" + sfx)
+    code = fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(g), _ptr(kv_lens), _ptr(cu_rows),
+              _ptr(tree_mask), _ptr(out), _ptr(lse), B, T, Hq, Hkv, Lcap, max_rows, max_kv_len,
+              _ptr(workspace), workspace.numel() * workspace.element_size(), _stream())
+    check(code, "gqa_attn_verify_tree" + sfx)
     return (out, lse) if return_lse else out
 
 
 def kv_append(k_new, v_new, kv_lens, k_cache, v_cache, cu_rows=None):
     """Writes new rows ([T,Hkv,256] bf16) after the kv_lens[b] keys each sequence
-    holds in the caches ([B,Hkv,Lcap,256]); kv_lens itself is not updated."""
+    holds in the caches ([B,Hkv,Lcap,256]); kv_lens itself is not updated.  The
+    copy moves 16-bit elements: bf16 or fp16, the same type throughout."""
+    _elem(k_cache, "k_cache")
     for t, n in ((k_new, "k_new"), (v_new, "v_new")):
-        _need(t, torch.bfloat16, 3, n)
-    _need(k_cache, torch.bfloat16, 4, "k_cache")
-    _need(v_cache, torch.bfloat16, 4, "v_cache")
+        _need(t, k_cache.dtype, 3, n)
+    _need(k_cache, k_cache.dtype, 4, "k_cache")
+    _need(v_cache, k_cache.dtype, 4, "v_cache")
     T, Hkv, _ = k_new.shape
     B, _, Lcap, _ = k_cache.shape
     check(load().gqa_kv_append(_ptr(k_new), _ptr(v_new), _ptr(cu_rows), _ptr(kv_lens),
@@ -165,9 +188,10 @@ def kv_append(k_new, v_new, kv_lens, k_cache, v_cache, cu_rows=None):
 def kv_keep(k_cache, v_cache, kv_lens, cu_rows, keep_idx, cu_keep, kv_lens_out=None):
     """Moves the accepted draft rows (keep_idx, per sequence via cu_keep, strictly
     increasing draft-row indices) to the front of each sequence's draft region, in
-    place; writes the new lengths into kv_lens_out when given."""
-    _need(k_cache, torch.bfloat16, 4, "k_cache")
-    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    place; writes the new lengths into kv_lens_out when given.  bf16 or fp16."""
+    _elem(k_cache, "k_cache")
+    _need(k_cache, k_cache.dtype, 4, "k_cache")
+    _need(v_cache, k_cache.dtype, 4, "v_cache")
     B, Hkv, Lcap, _ = k_cache.shape
     check(load().gqa_kv_keep(_ptr(k_cache), _ptr(v_cache), _ptr(kv_lens), _ptr(cu_rows),
                              _ptr(keep_idx), _ptr(cu_keep), _ptr(kv_lens_out), B, Hkv, Lcap,
@@ -176,10 +200,12 @@ def kv_keep(k_cache, v_cache, kv_lens, cu_rows, keep_idx, cu_keep, kv_lens_out=N
 
 def decode_split(q, k_cache, v_cache, kv_lens, cu_rows=None, max_rows=None, max_kv_len=None,
                  num_splits=None, split_keys=None, o_parts=None, lse_parts=None):
-    """First half of decode: partial results (O/l [S,T*Hq,256] fp32, lse [S,T*Hq])."""
-    _need(q, torch.bfloat16, 3, "q")
-    _need(k_cache, torch.bfloat16, 4, "k_cache")
-    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    """First half of decode: partial results (O/l [S,T*Hq,256] fp32, lse [S,T*Hq]).
+    bf16 or fp16 inputs."""
+    sfx = _elem(q, "q")
+    _need(q, q.dtype, 3, "q")
+    _need(k_cache, q.dtype, 4, "k_cache")
+    _need(v_cache, q.dtype, 4, "v_cache")
     T, Hq, B, Hkv, Lcap, max_rows, max_kv_len = _decode_sizes(q, k_cache, kv_lens, cu_rows,
                                                                max_rows, max_kv_len)
     if num_splits is None or split_keys is None:
@@ -188,17 +214,18 @@ def decode_split(q, k_cache, v_cache, kv_lens, cu_rows=None, max_rows=None, max_
         o_parts = torch.empty((num_splits, T * Hq, HEAD_DIM), dtype=torch.float32, device=q.device)
     if lse_parts is None:
         lse_parts = torch.empty((num_splits, T * Hq), dtype=torch.float32, device=q.device)
-    code = load().gqa_attn_decode_split(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_lens),
-                                        _ptr(cu_rows), _ptr(o_parts), _ptr(lse_parts), B, T, Hq,
-                                        Hkv, Lcap, max_rows, max_kv_len, num_splits, split_keys,
-                                        _stream())
-    check(code, "gqa_attn_decode_split")
+    fn = getattr(load(), "gqa_attn_decode_split" + sfx)
+    code = fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_lens), _ptr(cu_rows), _ptr(o_parts),
+              _ptr(lse_parts), B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, num_splits, split_keys,
+              _stream())
+    check(code, "gqa_attn_decode_split" + sfx)
     return o_parts, lse_parts
 
 
-def lse_merge(o_parts, lse_parts, g=None, out=None, return_lse=False):
+def lse_merge(o_parts, lse_parts, g=None, out=None, return_lse=False, dtype=None):
     """Merge S partial results: o_parts [S,N,256] fp32, lse_parts [S,N] fp32,
-    g None or [N,256] bf16 (any shape with N*256 elements).  Returns out [N,256] bf16."""
+    g None or [N,256] (any shape with N*256 elements).  Returns out [N,256] in the
+    element type `dtype` (bf16 or fp16; default: that of g, else of out, else bf16)."""
     if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
         raise TypeError("o_parts and lse_parts must be float32")
     if not (o_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_contiguous()):
@@ -206,15 +233,22 @@ def lse_merge(o_parts, lse_parts, g=None, out=None, return_lse=False):
     S, N, D = o_parts.shape
     if D != HEAD_DIM or tuple(lse_parts.shape) != (S, N):
         raise ValueError("shapes must be [S,N,256] and [S,N]")
-    if g is not None and (g.dtype != torch.bfloat16 or g.numel() != N * HEAD_DIM
+    if dtype is None:
+        dtype = g.dtype if g is not None else out.dtype if out is not None else torch.bfloat16
+    if dtype not in _ELEM:
+        raise TypeError(f"dtype must be bfloat16 or float16, got {dtype}")
+    sfx = _ELEM[dtype]
+    if g is not None and (g.dtype != dtype or g.numel() != N * HEAD_DIM
                           or not g.is_contiguous()):
-        raise ValueError("g must be contiguous bf16 with N*256 elements")
+        raise ValueError(f"g must be contiguous {dtype} with N*256 elements")
     if out is None:
-        out = torch.empty((N, HEAD_DIM), dtype=torch.bfloat16, device=o_parts.device)
+        out = torch.empty((N, HEAD_DIM), dtype=dtype, device=o_parts.device)
+    if out.dtype != dtype or out.numel() != N * HEAD_DIM or not out.is_contiguous():
+        raise ValueError(f"out must be contiguous {dtype} with N*256 elements")
     lse = torch.empty(N, dtype=torch.float32, device=o_parts.device) if return_lse else None
-    code = load().attn_lse_merge(_ptr(o_parts), _ptr(lse_parts), S, N, _ptr(g), _ptr(out),
-                                 _ptr(lse), _stream())
-    check(code, "attn_lse_merge")
+    fn = getattr(load(), "attn_lse_merge" + sfx)
+    code = fn(_ptr(o_parts), _ptr(lse_parts), S, N, _ptr(g), _ptr(out), _ptr(lse), _stream())
+    check(code, "attn_lse_merge" + sfx)
     return (out, lse) if return_lse else out
 
 

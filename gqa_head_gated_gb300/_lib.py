@@ -47,6 +47,9 @@ SIGNATURES = {
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      _P]),
 }
+for _name in ("gqa_attn_prefill", "gqa_attn_decode", "gqa_attn_verify_tree",
+              "gqa_attn_decode_split", "attn_lse_merge"):
+    SIGNATURES[_name + "_f16"] = SIGNATURES[_name]   # fp16 twins, same arguments
 
 _lib = None
 

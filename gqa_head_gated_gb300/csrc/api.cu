@@ -131,12 +131,13 @@ size_t workspace_bytes_for(int T, int Hq, int S) {
 int run_split(const void* Q, const void* Kc, const void* Vc, const int* kv_lens,
               const int* cu_rows, float* O_parts, float* lse_parts, int B, int T, int Hq, int Hkv,
               int Lcap, int max_rows, int max_kv_len, int S, int C, cudaStream_t stream,
-              const unsigned long long* tree_mask = nullptr) {
+              const unsigned long long* tree_mask, bool f16) {
   LaunchCtl ctl;
   if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
   DecodeSplitArgs a{Q, Kc, Vc, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
                     max_rows, max_kv_len, S, C};
   a.tree_mask = tree_mask;
+  a.f16 = f16;
   if (tc_path(Hq, Hkv, max_rows) && C % tc_split_keys_multiple() == 0) {
     bool encode_failed = false;
     const cudaError_t e = launch_decode_split_tc(a, ctl, stream, &encode_failed);
@@ -158,6 +159,139 @@ void decode_plan_current_device(int B, int Hq, int Hkv, int max_rows, int max_kv
 }
 size_t decode_workspace_bytes(int T, int Hq, int S) { return workspace_bytes_for(T, Hq, S); }
 bool make_launch_ctl(LaunchCtl* ctl) { return make_ctl(ctl); }
+
+namespace {
+
+// Entry points for both element types; the extern "C" functions below pick one.
+int gqa_attn_prefill_impl(bool f16, const void* Q, const void* K, const void* V, const void* G,
+                          void* out, float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv,
+                          int kv_offset, gqa_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq < 0 || Lkv < 1 || kv_offset < 0 ||
+      (long long)kv_offset + Lq > Lkv)
+    return GQA_ERR_INVALID_ARG;
+  if (Lq == 0) return GQA_OK;   // nothing to do (an empty tensor may have a null pointer)
+  if (Q == nullptr || K == nullptr || V == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 16) ||
+      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)))
+    return GQA_ERR_INVALID_ARG;
+  if (Hq / Hkv > 128) return GQA_ERR_UNSUPPORTED;
+  if ((long long)Hq * Lq >= (1LL << 31) || (long long)B * Hkv >= (1LL << 31))
+    return GQA_ERR_UNSUPPORTED;
+  const long long grid = (long long)ceil_div(Lq, prefill_rows_per_tile(Hq / Hkv)) * B * Hkv;
+  if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
+  LaunchCtl ctl;
+  if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
+  PrefillArgs a{Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset};
+  a.f16 = f16;
+  bool encode_failed = false;
+  const cudaError_t e = launch_prefill(a, ctl, static_cast<cudaStream_t>(stream), &encode_failed);
+  if (encode_failed) return GQA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+int gqa_attn_decode_split_impl(bool f16, const void* Q, const void* Kcache, const void* Vcache,
+                               const int* kv_lens, const int* cu_rows, float* O_parts,
+                               float* lse_parts, int B, int T, int Hq, int Hkv, int Lcap,
+                               int max_rows, int max_kv_len, int num_splits, int split_keys,
+                               gqa_stream_t stream) {
+  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
+  if (st != GQA_OK) return st;
+  if (num_splits < 1 || split_keys < 64 || split_keys % 64 != 0 ||
+      (long long)num_splits * split_keys < max_kv_len)
+    return GQA_ERR_INVALID_ARG;
+  if (T == 0) return GQA_OK;
+  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
+      O_parts == nullptr || lse_parts == nullptr)
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(O_parts, 16) ||
+      !aligned(lse_parts, 4) || !aligned(kv_lens, 4) || (cu_rows && !aligned(cu_rows, 4)))
+    return GQA_ERR_INVALID_ARG;
+  const int gqa = Hq / Hkv;
+  const long long packed = (long long)max_rows * gqa;
+  const int MB = decode_rows_per_cta(int(packed > (1 << 30) ? (1 << 30) : packed));
+  const long long grid = (long long)B * Hkv * num_splits * ((packed + MB - 1) / MB);
+  if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
+  return run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
+                   max_rows, max_kv_len, num_splits, split_keys,
+                   static_cast<cudaStream_t>(stream), nullptr, f16);
+}
+
+int attn_lse_merge_impl(bool f16, const float* O_parts, const float* lse_parts, int S, int N,
+                        const void* G, void* out, float* lse_out, gqa_stream_t stream) {
+  if (S < 1 || N < 0) return GQA_ERR_INVALID_ARG;
+  if (N == 0) return GQA_OK;
+  if (O_parts == nullptr || lse_parts == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
+  if (!aligned(O_parts, 16) || !aligned(lse_parts, 4) || !aligned(out, 16) ||
+      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)))
+    return GQA_ERR_INVALID_ARG;
+  LaunchCtl ctl;
+  if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
+  MergeArgs a{O_parts, lse_parts, S, N, G, out, lse_out};
+  a.f16 = f16;
+  return launch_lse_merge(a, ctl, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+int gqa_attn_decode_impl(bool f16, const void* Q, const void* Kcache, const void* Vcache,
+                         const void* G, const int* kv_lens, const int* cu_rows, void* out,
+                         float* lse_out, int B, int T, int Hq, int Hkv, int Lcap, int max_rows,
+                         int max_kv_len, void* workspace, size_t workspace_bytes,
+                         gqa_stream_t stream) {
+  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
+  if (st != GQA_OK) return st;
+  if (T == 0) return GQA_OK;
+  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
+      out == nullptr)
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || (G != nullptr && !aligned(G, 16)) ||
+      (lse_out != nullptr && !aligned(lse_out, 4)))
+    return GQA_ERR_INVALID_ARG;
+  int S = 0, C = 0;
+  plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
+  const size_t need = workspace_bytes_for(T, Hq, S);
+  if (workspace == nullptr || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return GQA_ERR_INVALID_ARG;
+  float* O_parts = static_cast<float*>(workspace);
+  float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
+  int r = gqa_attn_decode_split_impl(f16, Q, Kcache, Vcache, kv_lens, cu_rows, O_parts,
+                                     lse_parts, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, S, C,
+                                     stream);
+  if (r != GQA_OK) return r;
+  return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
+}
+
+int gqa_attn_verify_tree_impl(bool f16, const void* Q, const void* Kcache, const void* Vcache,
+                              const void* G, const int* kv_lens, const int* cu_rows,
+                              const unsigned long long* tree_mask, void* out, float* lse_out,
+                              int B, int T, int Hq, int Hkv, int Lcap, int max_rows,
+                              int max_kv_len, void* workspace, size_t workspace_bytes,
+                              gqa_stream_t stream) {
+  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
+  if (st != GQA_OK) return st;
+  if (max_rows > 64) return GQA_ERR_UNSUPPORTED;   // one 64-bit mask per row
+  if (T == 0) return GQA_OK;
+  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
+      cu_rows == nullptr || tree_mask == nullptr || out == nullptr)
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(out, 16) ||
+      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)) ||
+      !aligned(kv_lens, 4) || !aligned(cu_rows, 4) || !aligned(tree_mask, 8))
+    return GQA_ERR_INVALID_ARG;
+  int S = 0, C = 0;
+  plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
+  const size_t need = workspace_bytes_for(T, Hq, S);
+  if (workspace == nullptr || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return GQA_ERR_INVALID_ARG;
+  float* O_parts = static_cast<float*>(workspace);
+  float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
+  int r = run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
+                    max_rows, max_kv_len, S, C, static_cast<cudaStream_t>(stream), tree_mask, f16);
+  if (r != GQA_OK) return r;
+  return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
+}
+
+}  // namespace
 
 }  // namespace gqa
 
@@ -187,26 +321,14 @@ void gqa_set_wait_timeout_ns(unsigned long long ns) {
 int gqa_attn_prefill(const void* Q, const void* K, const void* V, const void* G, void* out,
                      float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv, int kv_offset,
                      gqa_stream_t stream) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq < 0 || Lkv < 1 || kv_offset < 0 ||
-      (long long)kv_offset + Lq > Lkv)
-    return GQA_ERR_INVALID_ARG;
-  if (Lq == 0) return GQA_OK;   // nothing to do (an empty tensor may have a null pointer)
-  if (Q == nullptr || K == nullptr || V == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
-  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 16) ||
-      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)))
-    return GQA_ERR_INVALID_ARG;
-  if (Hq / Hkv > 128) return GQA_ERR_UNSUPPORTED;
-  if ((long long)Hq * Lq >= (1LL << 31) || (long long)B * Hkv >= (1LL << 31))
-    return GQA_ERR_UNSUPPORTED;
-  const long long grid = (long long)ceil_div(Lq, prefill_rows_per_tile(Hq / Hkv)) * B * Hkv;
-  if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
-  LaunchCtl ctl;
-  if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
-  PrefillArgs a{Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset};
-  bool encode_failed = false;
-  const cudaError_t e = launch_prefill(a, ctl, static_cast<cudaStream_t>(stream), &encode_failed);
-  if (encode_failed) return GQA_ERR_UNSUPPORTED;
-  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  return gqa_attn_prefill_impl(false, Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset,
+                               stream);
+}
+int gqa_attn_prefill_f16(const void* Q, const void* K, const void* V, const void* G, void* out,
+                         float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv, int kv_offset,
+                         gqa_stream_t stream) {
+  return gqa_attn_prefill_impl(true, Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset,
+                               stream);
 }
 
 int gqa_attn_decode_plan(int B, int T, int Hq, int Hkv, int max_rows, int max_kv_len,
@@ -228,68 +350,44 @@ int gqa_attn_decode_split(const void* Q, const void* Kcache, const void* Vcache,
                           const int* kv_lens, const int* cu_rows, float* O_parts,
                           float* lse_parts, int B, int T, int Hq, int Hkv, int Lcap, int max_rows,
                           int max_kv_len, int num_splits, int split_keys, gqa_stream_t stream) {
-  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
-  if (st != GQA_OK) return st;
-  if (num_splits < 1 || split_keys < 64 || split_keys % 64 != 0 ||
-      (long long)num_splits * split_keys < max_kv_len)
-    return GQA_ERR_INVALID_ARG;
-  if (T == 0) return GQA_OK;
-  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
-      O_parts == nullptr || lse_parts == nullptr)
-    return GQA_ERR_INVALID_ARG;
-  if (!aligned(Q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(O_parts, 16) ||
-      !aligned(lse_parts, 4) || !aligned(kv_lens, 4) || (cu_rows && !aligned(cu_rows, 4)))
-    return GQA_ERR_INVALID_ARG;
-  const int gqa = Hq / Hkv;
-  const long long packed = (long long)max_rows * gqa;
-  const int MB = decode_rows_per_cta(int(packed > (1 << 30) ? (1 << 30) : packed));
-  const long long grid = (long long)B * Hkv * num_splits * ((packed + MB - 1) / MB);
-  if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
-  return run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
-                   max_rows, max_kv_len, num_splits, split_keys,
-                   static_cast<cudaStream_t>(stream));
+  return gqa_attn_decode_split_impl(false, Q, Kcache, Vcache, kv_lens, cu_rows, O_parts,
+                                    lse_parts, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len,
+                                    num_splits, split_keys, stream);
+}
+int gqa_attn_decode_split_f16(const void* Q, const void* Kcache, const void* Vcache,
+                              const int* kv_lens, const int* cu_rows, float* O_parts,
+                              float* lse_parts, int B, int T, int Hq, int Hkv, int Lcap,
+                              int max_rows, int max_kv_len, int num_splits, int split_keys,
+                              gqa_stream_t stream) {
+  return gqa_attn_decode_split_impl(true, Q, Kcache, Vcache, kv_lens, cu_rows, O_parts,
+                                    lse_parts, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len,
+                                    num_splits, split_keys, stream);
 }
 
 int attn_lse_merge(const float* O_parts, const float* lse_parts, int S, int N, const void* G,
                    void* out, float* lse_out, gqa_stream_t stream) {
-  if (S < 1 || N < 0) return GQA_ERR_INVALID_ARG;
-  if (N == 0) return GQA_OK;
-  if (O_parts == nullptr || lse_parts == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
-  if (!aligned(O_parts, 16) || !aligned(lse_parts, 4) || !aligned(out, 16) ||
-      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)))
-    return GQA_ERR_INVALID_ARG;
-  LaunchCtl ctl;
-  if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
-  MergeArgs a{O_parts, lse_parts, S, N, G, out, lse_out};
-  return launch_lse_merge(a, ctl, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? GQA_OK
-             : GQA_ERR_CUDA;
+  return attn_lse_merge_impl(false, O_parts, lse_parts, S, N, G, out, lse_out, stream);
+}
+int attn_lse_merge_f16(const float* O_parts, const float* lse_parts, int S, int N, const void* G,
+                       void* out, float* lse_out, gqa_stream_t stream) {
+  return attn_lse_merge_impl(true, O_parts, lse_parts, S, N, G, out, lse_out, stream);
 }
 
 int gqa_attn_decode(const void* Q, const void* Kcache, const void* Vcache, const void* G,
                     const int* kv_lens, const int* cu_rows, void* out, float* lse_out, int B,
                     int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
                     void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
-  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
-  if (st != GQA_OK) return st;
-  if (T == 0) return GQA_OK;
-  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
-      out == nullptr)
-    return GQA_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || (G != nullptr && !aligned(G, 16)) ||
-      (lse_out != nullptr && !aligned(lse_out, 4)))
-    return GQA_ERR_INVALID_ARG;
-  int S = 0, C = 0;
-  plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
-  const size_t need = workspace_bytes_for(T, Hq, S);
-  if (workspace == nullptr || workspace_bytes < need) return GQA_ERR_WORKSPACE;
-  if (!aligned(workspace, 16)) return GQA_ERR_INVALID_ARG;
-  float* O_parts = static_cast<float*>(workspace);
-  float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
-  int r = gqa_attn_decode_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq,
-                                Hkv, Lcap, max_rows, max_kv_len, S, C, stream);
-  if (r != GQA_OK) return r;
-  return attn_lse_merge(O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
+  return gqa_attn_decode_impl(false, Q, Kcache, Vcache, G, kv_lens, cu_rows, out, lse_out, B, T,
+                              Hq, Hkv, Lcap, max_rows, max_kv_len, workspace, workspace_bytes,
+                              stream);
+}
+int gqa_attn_decode_f16(const void* Q, const void* Kcache, const void* Vcache, const void* G,
+                        const int* kv_lens, const int* cu_rows, void* out, float* lse_out, int B,
+                        int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                        void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+  return gqa_attn_decode_impl(true, Q, Kcache, Vcache, G, kv_lens, cu_rows, out, lse_out, B, T,
+                              Hq, Hkv, Lcap, max_rows, max_kv_len, workspace, workspace_bytes,
+                              stream);
 }
 
 int gqa_attn_verify_tree(const void* Q, const void* Kcache, const void* Vcache, const void* G,
@@ -297,28 +395,19 @@ int gqa_attn_verify_tree(const void* Q, const void* Kcache, const void* Vcache, 
                          const unsigned long long* tree_mask, void* out, float* lse_out, int B,
                          int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
                          void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
-  const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
-  if (st != GQA_OK) return st;
-  if (max_rows > 64) return GQA_ERR_UNSUPPORTED;   // one 64-bit mask per row
-  if (T == 0) return GQA_OK;
-  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
-      cu_rows == nullptr || tree_mask == nullptr || out == nullptr)
-    return GQA_ERR_INVALID_ARG;
-  if (!aligned(Q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(out, 16) ||
-      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)) ||
-      !aligned(kv_lens, 4) || !aligned(cu_rows, 4) || !aligned(tree_mask, 8))
-    return GQA_ERR_INVALID_ARG;
-  int S = 0, C = 0;
-  plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
-  const size_t need = workspace_bytes_for(T, Hq, S);
-  if (workspace == nullptr || workspace_bytes < need) return GQA_ERR_WORKSPACE;
-  if (!aligned(workspace, 16)) return GQA_ERR_INVALID_ARG;
-  float* O_parts = static_cast<float*>(workspace);
-  float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
-  int r = run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
-                    max_rows, max_kv_len, S, C, static_cast<cudaStream_t>(stream), tree_mask);
-  if (r != GQA_OK) return r;
-  return attn_lse_merge(O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
+  return gqa_attn_verify_tree_impl(false, Q, Kcache, Vcache, G, kv_lens, cu_rows, tree_mask, out,
+                                   lse_out, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, workspace,
+                                   workspace_bytes, stream);
+}
+int gqa_attn_verify_tree_f16(const void* Q, const void* Kcache, const void* Vcache,
+                             const void* G, const int* kv_lens, const int* cu_rows,
+                             const unsigned long long* tree_mask, void* out, float* lse_out,
+                             int B, int T, int Hq, int Hkv, int Lcap, int max_rows,
+                             int max_kv_len, void* workspace, size_t workspace_bytes,
+                             gqa_stream_t stream) {
+  return gqa_attn_verify_tree_impl(true, Q, Kcache, Vcache, G, kv_lens, cu_rows, tree_mask, out,
+                                   lse_out, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, workspace,
+                                   workspace_bytes, stream);
 }
 
 int gqa_last_device_status(gqa_stream_t stream) {

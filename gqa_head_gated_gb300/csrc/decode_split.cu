@@ -13,8 +13,9 @@
 // cp.async ring (two CTAs per SM for up to 32 packed rows) with 16-byte vector
 // copies, coalesced along the 512-byte rows;
 // rows at or past the split's end are zero-filled by the copy itself, so cache
-// padding is never read.  Scores and P.V run on bf16 mma.sync (m16n8k16,
-// fp32 accumulate); the online softmax is fp32 with quad-shuffle row reductions.
+// padding is never read.  Scores and P.V run on bf16 or fp16 mma.sync (m16n8k16,
+// fp32 accumulate); the online softmax is fp32 with quad-shuffle row reductions
+// and rescales at every tile, so P <= 1 in either element type.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -26,13 +27,13 @@ namespace {
 constexpr int kTK = 32;          // keys per tile
 constexpr int kStages = 3;
 constexpr int kThreads = 128;
-constexpr int kRowBytes = 512;   // 256 bf16
+constexpr int kRowBytes = 512;   // 256 16-bit elements
 constexpr int kTileBytes = kTK * kRowBytes;   // one of K or V
 
 struct Params {
-  const __nv_bfloat16* Q;
-  const __nv_bfloat16* K;
-  const __nv_bfloat16* V;
+  const uint16_t* Q;   // bf16 or fp16 bits
+  const uint16_t* K;
+  const uint16_t* V;
   const int* kv_lens;
   const int* cu_rows;
   const unsigned long long* tree_mask;   // null: chain verify
@@ -79,13 +80,22 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+template <bool kF16>
+__device__ __forceinline__ void mma_16b(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (kF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -95,7 +105,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // WR row groups of 16 packed rows; WK key groups per row group (WR * WK warps).
-template <int WR, int WK>
+template <int WR, int WK, bool kF16>
 __global__ void __launch_bounds__(kThreads)
 decode_split_kernel(const Params p) {
   constexpr int MB = 16 * WR;          // packed rows per CTA
@@ -163,8 +173,8 @@ decode_split_kernel(const Params p) {
   const int n_tiles = n_hi > k_lo ? (n_hi - k_lo + kTK - 1) / kTK : 0;
 
   const size_t kv_base = (size_t(b) * p.Hkv + g) * size_t(p.Lcap) * 256;
-  const __nv_bfloat16* Kg = p.K + kv_base;
-  const __nv_bfloat16* Vg = p.V + kv_base;
+  const uint16_t* Kg = p.K + kv_base;
+  const uint16_t* Vg = p.V + kv_base;
 
   // Q block: packed row pp -> token t0 + pp / gqa, head g*gqa + pp % gqa.
   {
@@ -173,7 +183,7 @@ decode_split_kernel(const Params p) {
       const int r = c >> 5, ch = c & 31;
       const int pp = p0 + r;
       const bool ok = pp < P;
-      const __nv_bfloat16* src =
+      const uint16_t* src =
           ok ? p.Q + ((size_t(t0 + pp / p.gqa) * p.Hq) + g * p.gqa + pp % p.gqa) * 256 + ch * 8
              : p.Q;
       cp_async16(q0 + swz(r, ch), src, ok ? 16u : 0u);
@@ -250,8 +260,8 @@ decode_split_kernel(const Params p) {
         const int r = wk * NK + np * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int ch = 2 * kk + ((lane >> 3) & 1);
         ldsm_x4(kb + swz(r, ch), b0, b1, b2, b3);
-        mma_bf16(sc2[kk % KC][2 * np], a0, a1, a2, a3, b0, b1);
-        mma_bf16(sc2[kk % KC][2 * np + 1], a0, a1, a2, a3, b2, b3);
+        mma_16b<kF16>(sc2[kk % KC][2 * np], a0, a1, a2, a3, b0, b1);
+        mma_16b<kF16>(sc2[kk % KC][2 * np + 1], a0, a1, a2, a3, b2, b3);
       }
     }
 #pragma unroll
@@ -308,18 +318,18 @@ decode_split_kernel(const Params p) {
     // O += P V over this warp's keys.
 #pragma unroll
     for (int ks = 0; ks < NK / 16; ++ks) {
-      const uint32_t pa0 = pack_bf16x2(sc[2 * ks][0], sc[2 * ks][1]);
-      const uint32_t pa1 = pack_bf16x2(sc[2 * ks][2], sc[2 * ks][3]);
-      const uint32_t pa2 = pack_bf16x2(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-      const uint32_t pa3 = pack_bf16x2(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+      const uint32_t pa0 = pack_elem2<kF16>(sc[2 * ks][0], sc[2 * ks][1]);
+      const uint32_t pa1 = pack_elem2<kF16>(sc[2 * ks][2], sc[2 * ks][3]);
+      const uint32_t pa2 = pack_elem2<kF16>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+      const uint32_t pa3 = pack_elem2<kF16>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
       const int r = wk * NK + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
       for (int dp = 0; dp < 16; ++dp) {
         uint32_t b0, b1, b2, b3;
         const int ch = 2 * dp + (lane >> 4);
         ldsm_x4_t(vb + swz(r, ch), b0, b1, b2, b3);
-        mma_bf16(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
-        mma_bf16(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+        mma_16b<kF16>(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
+        mma_16b<kF16>(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
       }
     }
   }
@@ -357,15 +367,14 @@ decode_split_kernel(const Params p) {
     const int pp = p0 + r;
     const size_t n = size_t(t0 + pp / p.gqa) * p.Hq + g * p.gqa + pp % p.gqa;
     const size_t part = size_t(s) * size_t(p.T) * p.Hq + n;
-    if (M == -INFINITY) {
-      if (c4 == 0) p.lse_parts[part] = -INFINITY;
-      continue;
-    }
+    // fmaxf drops NaN scores, so a row that saw only NaN keeps M = -inf; it is
+    // told apart from a row that saw no key by its sum (NaN, not 0).
+    const float Msub = M == -INFINITY ? 0.f : M;
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < WK; ++k) {
-      const float w = ex2(s_m[k][r] - M);
+      const float w = ex2(s_m[k][r] - Msub);
       L += w * s_l[k][r];
       const float4 v = *reinterpret_cast<const float4*>(sO + (size_t(k) * MB + r) * 256 + c4);
       acc.x += w * v.x;
@@ -373,24 +382,28 @@ decode_split_kernel(const Params p) {
       acc.z += w * v.z;
       acc.w += w * v.w;
     }
+    if (L == 0.f) {   // no key of this split is visible to the row
+      if (c4 == 0) p.lse_parts[part] = -INFINITY;
+      continue;
+    }
     const float inv = 1.f / L;
     acc.x *= inv;
     acc.y *= inv;
     acc.z *= inv;
     acc.w *= inv;
     *reinterpret_cast<float4*>(p.O_parts + part * 256 + c4) = acc;
-    if (c4 == 0) p.lse_parts[part] = (M + __log2f(L)) * kLn2;
+    if (c4 == 0) p.lse_parts[part] = (Msub + __log2f(L)) * kLn2;
   }
 }
 
-template <int WR, int WK>
+template <int WR, int WK, bool kF16>
 cudaError_t launch_t(const Params& p, cudaStream_t stream, long long grid) {
   constexpr int MB = 16 * WR;
   const size_t smem = size_t(MB) * kRowBytes + size_t(kStages) * 2 * kTileBytes;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<WR, WK>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<WR, WK, kF16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  decode_split_kernel<WR, WK><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(p);
+  decode_split_kernel<WR, WK, kF16><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -405,9 +418,9 @@ int decode_rows_per_cta(int packed_rows) {
 cudaError_t launch_decode_split(const DecodeSplitArgs& a, const LaunchCtl& ctl,
                                 cudaStream_t stream) {
   Params p;
-  p.Q = static_cast<const __nv_bfloat16*>(a.Q);
-  p.K = static_cast<const __nv_bfloat16*>(a.K);
-  p.V = static_cast<const __nv_bfloat16*>(a.V);
+  p.Q = static_cast<const uint16_t*>(a.Q);
+  p.K = static_cast<const uint16_t*>(a.K);
+  p.V = static_cast<const uint16_t*>(a.V);
   p.kv_lens = a.kv_lens;
   p.cu_rows = a.cu_rows;
   p.tree_mask = a.tree_mask;
@@ -427,9 +440,14 @@ cudaError_t launch_decode_split(const DecodeSplitArgs& a, const LaunchCtl& ctl,
   const int MB = decode_rows_per_cta(a.max_rows * p.gqa);
   p.n_rb = (a.max_rows * p.gqa + MB - 1) / MB;
   const long long grid = (long long)a.B * a.Hkv * a.num_splits * p.n_rb;
-  if (MB == 16) return launch_t<1, 2>(p, stream, grid);
-  if (MB == 32) return launch_t<2, 2>(p, stream, grid);
-  return launch_t<4, 1>(p, stream, grid);
+  if (a.f16) {
+    if (MB == 16) return launch_t<1, 2, true>(p, stream, grid);
+    if (MB == 32) return launch_t<2, 2, true>(p, stream, grid);
+    return launch_t<4, 1, true>(p, stream, grid);
+  }
+  if (MB == 16) return launch_t<1, 2, false>(p, stream, grid);
+  if (MB == 32) return launch_t<2, 2, false>(p, stream, grid);
+  return launch_t<4, 1, false>(p, stream, grid);
 }
 
 }  // namespace gqa

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "gqa_attn.h"
@@ -37,6 +38,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
   return __bfloat1622float2(v);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_half2(uint32_t u) {
+  __half2 v = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(v);
+}
+
+// Two 16-bit elements of the kernels' element type (fp16 or bf16) <-> float2.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_elem2(float lo, float hi) {
+  if constexpr (kF16) return pack_half2(lo, hi); else return pack_bf16x2(lo, hi);
+}
+template <bool kF16>
+__device__ __forceinline__ float2 unpack_elem2(uint32_t u) {
+  if constexpr (kF16) return unpack_half2(u); else return unpack_bf16x2(u);
 }
 
 // Logistic function for the output gate, fp32.

@@ -17,6 +17,7 @@ struct PrefillArgs {
   void* out;
   float* lse;
   int B, Hq, Hkv, Lq, Lkv, kv_offset;
+  bool f16 = false;   // fp16 instead of bf16 elements
 };
 
 // Rows of one prefill tile: floor(128 / GQA) query rows of every head in the group.
@@ -39,6 +40,7 @@ struct DecodeSplitArgs {
   // Tree verify: per new row, a mask over its sequence's new rows (bit k = new row
   // k visible); null for chain verify / decode.
   const unsigned long long* tree_mask = nullptr;
+  bool f16 = false;   // fp16 instead of bf16 elements
 };
 
 // Packed query rows (heads x rows of one KV group) per decode CTA: 16, 32 or 64.
@@ -61,6 +63,7 @@ struct MergeArgs {
   const void* G;
   void* out;
   float* lse_out;
+  bool f16 = false;   // fp16 instead of bf16 G / out
 };
 
 cudaError_t launch_lse_merge(const MergeArgs& a, const LaunchCtl& ctl, cudaStream_t stream);

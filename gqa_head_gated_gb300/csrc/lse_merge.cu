@@ -1,5 +1,6 @@
 // attn_lse_merge: combine S partial attention results of the same rows computed
-// over disjoint key sets, then apply the sigmoid output gate and round to bf16.
+// over disjoint key sets, then apply the sigmoid output gate and round to bf16
+// (or fp16: the gate and output element type is a template flag).
 //
 //   out[n,:] = sum_s exp(lse_s - M) O_s[n,:] / sum_s exp(lse_s - M) * sigmoid(G[n,:])
 //   lse[n]   = M + ln sum_s exp(lse_s - M),   M = max_s lse_s
@@ -7,8 +8,9 @@
 // This is the tail-chunk merge of the TensorFold PR #1009 attention contract
 // ("Receipt": decode over cache chunks, then a merge; its control "a merge
 // dropping later tail chunks" must fail).  Parts with lse = -inf carry weight 0
-// and their O rows are never read.  One warp per row; each lane owns 8 of the
-// 256 columns and reads them as two float4 per part.
+// and their O rows are never read.  A NaN lse (a part that saw a NaN score)
+// makes the row NaN, as float64 arithmetic of the formula would.  One warp per
+// row; each lane owns 8 of the 256 columns and reads them as two float4 per part.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -19,16 +21,18 @@ namespace {
 
 constexpr int kWarps = 8;
 
+template <bool kF16>
 __global__ void __launch_bounds__(kWarps * 32)
 lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ lse_parts, int S,
-                 int N, const __nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__ out,
+                 int N, const uint16_t* __restrict__ G, uint16_t* __restrict__ out,
                  float* __restrict__ lse_out) {
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (n >= N) return;
   const size_t stride = size_t(N);
 
-  // Max over parts, 32 parts per round (lane s reads part s of the round).
+  // Max over parts, 32 parts per round (lane s reads part s of the round).  fmaxf
+  // drops NaN; a NaN part still gets weight NaN below.
   float M = -INFINITY;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse_parts + size_t(s) * stride + n));
 #pragma unroll
@@ -37,12 +41,13 @@ lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ ls
   const int c0 = lane * 8;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
-  if (M != -INFINITY) {
+  const float Msub = M == -INFINITY ? 0.f : M;
+  {
     for (int s0 = 0; s0 < S; s0 += 32) {
       // lane s holds the weight of part s0 + s (0 for an empty or missing part)
       const int sl = s0 + lane;
       const float ls = sl < S ? __ldg(lse_parts + size_t(sl) * stride + n) : -INFINITY;
-      const float wl = ls == -INFINITY ? 0.f : __expf(ls - M);
+      const float wl = ls == -INFINITY ? 0.f : __expf(ls - Msub);
       const int cnt = min(32, S - s0);
       // Batches of 4 parts: the loads of a batch are issued together.
       for (int b = 0; b < cnt; b += 4) {
@@ -75,14 +80,14 @@ lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ ls
       }
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const float inv = wsum == 0.f ? 0.f : 1.f / wsum;
   float gs[8];
   if (G != nullptr) {
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(G + size_t(n) * 256 + c0));
     const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 f = unpack_bf16x2(w4[e]);
+      const float2 f = unpack_elem2<kF16>(w4[e]);
       gs[2 * e] = gate_sigmoid(f.x);
       gs[2 * e + 1] = gate_sigmoid(f.y);
     }
@@ -91,13 +96,13 @@ lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ ls
     for (int e = 0; e < 8; ++e) gs[e] = 1.f;
   }
   uint4 o;
-  o.x = pack_bf16x2(acc[0] * inv * gs[0], acc[1] * inv * gs[1]);
-  o.y = pack_bf16x2(acc[2] * inv * gs[2], acc[3] * inv * gs[3]);
-  o.z = pack_bf16x2(acc[4] * inv * gs[4], acc[5] * inv * gs[5]);
-  o.w = pack_bf16x2(acc[6] * inv * gs[6], acc[7] * inv * gs[7]);
+  o.x = pack_elem2<kF16>(acc[0] * inv * gs[0], acc[1] * inv * gs[1]);
+  o.y = pack_elem2<kF16>(acc[2] * inv * gs[2], acc[3] * inv * gs[3]);
+  o.z = pack_elem2<kF16>(acc[4] * inv * gs[4], acc[5] * inv * gs[5]);
+  o.w = pack_elem2<kF16>(acc[6] * inv * gs[6], acc[7] * inv * gs[7]);
   *reinterpret_cast<uint4*>(out + size_t(n) * 256 + c0) = o;
   if (lse_out != nullptr && lane == 0)
-    lse_out[n] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
+    lse_out[n] = wsum == 0.f ? -INFINITY : Msub + __logf(wsum);
 }
 
 }  // namespace
@@ -105,9 +110,14 @@ lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ ls
 cudaError_t launch_lse_merge(const MergeArgs& a, const LaunchCtl& ctl, cudaStream_t stream) {
   (void)ctl;
   const long long grid = (a.N + kWarps - 1) / kWarps;
-  lse_merge_kernel<<<dim3(unsigned(grid)), dim3(kWarps * 32), 0, stream>>>(
-      a.O_parts, a.lse_parts, a.S, a.N, static_cast<const __nv_bfloat16*>(a.G),
-      static_cast<__nv_bfloat16*>(a.out), a.lse_out);
+  const auto* G = static_cast<const uint16_t*>(a.G);
+  auto* out = static_cast<uint16_t*>(a.out);
+  if (a.f16)
+    lse_merge_kernel<true><<<dim3(unsigned(grid)), dim3(kWarps * 32), 0, stream>>>(
+        a.O_parts, a.lse_parts, a.S, a.N, G, out, a.lse_out);
+  else
+    lse_merge_kernel<false><<<dim3(unsigned(grid)), dim3(kWarps * 32), 0, stream>>>(
+        a.O_parts, a.lse_parts, a.S, a.N, G, out, a.lse_out);
   return cudaGetLastError();
 }
 

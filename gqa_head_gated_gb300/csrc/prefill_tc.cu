@@ -82,10 +82,15 @@ constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmO = 0;
 constexpr uint32_t kTmS = 256;                // S buffer b at kTmS + kN*b
-constexpr float kRescaleThreshold = 32.0f;    // log2 units
+// Lazy-rescale threshold in log2 units: P <= 2^threshold must fit the element type
+// (bf16: 2^32, fp16: 2^8, below its 65504 maximum).
+template <bool kF16>
+__device__ __forceinline__ float rescale_threshold() { return kF16 ? 8.0f : 32.0f; }
 
-constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kM, kN, 0, 0);    // Q, K both K-major
-constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kM, 256, 0, 1);  // V is MN-major
+template <bool kF16>
+constexpr uint32_t idesc_s() { return ptx::idesc_f32acc(kM, kN, 0, 0, kF16 ? 0u : 1u); }   // Q, K K-major
+template <bool kF16>
+constexpr uint32_t idesc_pv() { return ptx::idesc_f32acc(kM, 256, 0, 1, kF16 ? 0u : 1u); } // V MN-major
 
 struct __align__(1024) Smem {
   uint8_t q[kQBytes];
@@ -107,8 +112,8 @@ struct __align__(1024) Smem {
 };
 
 struct Params {
-  const __nv_bfloat16* G;
-  __nv_bfloat16* out;
+  const uint16_t* G;        // bf16 or fp16 bits
+  uint16_t* out;
   float* lse;
   int B, Hq, Hkv, Lq, kv_offset, gqa, R, n_rtiles;
   // split mode
@@ -164,7 +169,7 @@ __device__ __forceinline__ void item_kind(int it, int n, bool& is_v, int& j) {
   }
 }
 
-template <bool kSplit>
+template <bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -350,7 +355,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           const uint32_t qo = uint32_t(kk >> 2) * kQChunk + uint32_t(kk & 3) * 32u;
           const uint32_t ko = uint32_t(kk >> 2) * kChunkBytes + uint32_t(kk & 3) * 32u;
           ptx::mma_ss(d, ptx::sdesc_sw128(qa + qo, 16, 1024), ptx::sdesc_sw128(ka + ko, 16, 1024),
-                      kIdescS, kk > 0);
+                      idesc_s<kF16>(), kk > 0);
         }
         ptx::tc_commit(&sm.s_full[j & 1]);
         ptx::tc_commit(&sm.kv_empty[slot]);
@@ -375,7 +380,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           // P of keys 16kk..16kk+15: half kk / kStepsHalf, 8 columns per k16 step
           const uint32_t acol = uint32_t(kk / kStepsHalf) * kHalf + uint32_t(kk % kStepsHalf) * 8u;
           ptx::mma_ts(tmem + kTmO, pa + acol,
-                      ptx::sdesc_sw128(va + uint32_t(kk) * 2048u, kChunkBytes, 1024), kIdescPV,
+                      ptx::sdesc_sw128(va + uint32_t(kk) * 2048u, kChunkBytes, 1024), idesc_pv<kF16>(),
                       (j > 0 || kk > 0) ? 1u : 0u);
         }
         ptx::tc_commit(&sm.pv_done);
@@ -474,12 +479,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       bool store_ok = true;
       if (j == 0) {
         m_run = tmax;
-      } else if (__any_sync(0xffffffffu, tmax > m_run + kRescaleThreshold)) {
+      } else if (__any_sync(0xffffffffu, tmax > m_run + rescale_threshold<kF16>())) {
         // The branch is warp-uniform (tcgen05.ld/st are warp-collective; the partner warp
         // holds the same rows, so it takes it too), but only rows whose own max rose past
         // the threshold move it; the others multiply by exactly 1, so every row's result
         // depends on its own scores alone.
-        const bool need = tmax > m_run + kRescaleThreshold;
+        const bool need = tmax > m_run + rescale_threshold<kF16>();
         const float alpha = need ? ex2(m_run - tmax) : 1.f;
         if (need) m_run = tmax;
         l_part *= alpha;
@@ -510,7 +515,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), kScaleLog2, -msub));
         const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), kScaleLog2, -msub));
         ls4[c & 3] += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        pk[c] = pack_elem2<kF16>(p0, p1);
       }
       l_part += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       const uint32_t pdst = trow + kTmS + uint32_t(kN) * buf + uint32_t(kHalf) * half;
@@ -535,7 +540,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (fin) {
       ptx::tc_fence_after();
       const float l_tot = l_part + sm.red[pb][half ^ 1][row];
-      const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      // l_tot is 0 exactly when the row saw no key, NaN when it saw a NaN score.
+      const float inv_l = l_tot == 0.f ? 0.f : 1.f / l_tot;
       if constexpr (!kSplit) {
         const int h = g * p.gqa + hh;
         const size_t row_off = (size_t(b) * p.Hq + h) * size_t(p.Lq) + size_t(q);
@@ -554,7 +560,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  const float2 f = unpack_bf16x2(w[e]);
+                  const float2 f = unpack_elem2<kF16>(w[e]);
                   gs[v * 8 + 2 * e] = gate_sigmoid(f.x);
                   gs[v * 8 + 2 * e + 1] = gate_sigmoid(f.y);
                 }
@@ -567,25 +573,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(o[v * 8 + 0]) * inv_l * gs[v * 8 + 0],
+              u.x = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 0]) * inv_l * gs[v * 8 + 0],
                                 __uint_as_float(o[v * 8 + 1]) * inv_l * gs[v * 8 + 1]);
-              u.y = pack_bf16x2(__uint_as_float(o[v * 8 + 2]) * inv_l * gs[v * 8 + 2],
+              u.y = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 2]) * inv_l * gs[v * 8 + 2],
                                 __uint_as_float(o[v * 8 + 3]) * inv_l * gs[v * 8 + 3]);
-              u.z = pack_bf16x2(__uint_as_float(o[v * 8 + 4]) * inv_l * gs[v * 8 + 4],
+              u.z = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 4]) * inv_l * gs[v * 8 + 4],
                                 __uint_as_float(o[v * 8 + 5]) * inv_l * gs[v * 8 + 5]);
-              u.w = pack_bf16x2(__uint_as_float(o[v * 8 + 6]) * inv_l * gs[v * 8 + 6],
+              u.w = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 6]) * inv_l * gs[v * 8 + 6],
                                 __uint_as_float(o[v * 8 + 7]) * inv_l * gs[v * 8 + 7]);
               op[v] = u;
             }
           }
         }
         if (valid && half == 0 && p.lse != nullptr)
-          p.lse[row_off] = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
+          p.lse[row_off] = l_tot == 0.f ? -INFINITY : (m_run + __log2f(l_tot)) * kLn2;
       } else {
         // Normalised partial O / l (fp32) and lse for the merge; -inf: no key seen.
         const size_t n = size_t(t0 + q) * p.Hq + size_t(g) * p.gqa + hh;
         const size_t part = size_t(s_idx) * size_t(p.T) * p.Hq + n;
-        const bool live = valid && l_tot > 0.f;
+        const bool live = valid && l_tot != 0.f;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
@@ -636,14 +642,26 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-bool encode_bf16(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank,
-                 const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+bool encode_16b(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank,
+                const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                bool f16) {
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base),
+  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base),
                   dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+template <bool kSplit, bool kF16>
+cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const Params& p, long long grid, cudaStream_t stream) {
+  const size_t smem = sizeof(Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kSplit, kF16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  attn_tc_kernel<kSplit, kF16><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -663,21 +681,21 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
     const cuuint64_t dims[4] = {256, cuuint64_t(a.Lq), cuuint64_t(a.Hq), cuuint64_t(a.B)};
     const cuuint64_t str[3] = {512, cuuint64_t(a.Lq) * 512, cuuint64_t(a.Hq) * a.Lq * 512};
     const cuuint32_t box[4] = {64, cuuint32_t(R), cuuint32_t(gqa), 1};
-    if (!encode_bf16(fn, &tq, a.Q, 4, dims, str, box)) *encode_failed = true;
+    if (!encode_16b(fn, &tq, a.Q, 4, dims, str, box, a.f16)) *encode_failed = true;
   }
   {
     // Only keys a row of the call can see are addressable; TMA zero-fills the rest.
     const cuuint64_t dims[3] = {256, cuuint64_t(a.kv_offset + a.Lq), cuuint64_t(a.B) * a.Hkv};
     const cuuint64_t str[2] = {512, cuuint64_t(a.Lkv) * 512};
     const cuuint32_t box[3] = {64, cuuint32_t(kN), 1};   // one column block of a tile
-    if (!encode_bf16(fn, &tk, a.K, 3, dims, str, box)) *encode_failed = true;
-    if (!encode_bf16(fn, &tv, a.V, 3, dims, str, box)) *encode_failed = true;
+    if (!encode_16b(fn, &tk, a.K, 3, dims, str, box, a.f16)) *encode_failed = true;
+    if (!encode_16b(fn, &tv, a.V, 3, dims, str, box, a.f16)) *encode_failed = true;
   }
   if (*encode_failed) return cudaErrorInvalidValue;
 
   Params p{};
-  p.G = static_cast<const __nv_bfloat16*>(a.G);
-  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.G = static_cast<const uint16_t*>(a.G);
+  p.out = static_cast<uint16_t*>(a.out);
   p.lse = a.lse;
   p.B = a.B;
   p.Hq = a.Hq;
@@ -689,13 +707,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
   p.n_rtiles = (a.Lq + R - 1) / R;
   p.ctl = ctl;
 
-  const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e != cudaSuccess) return e;
   const long long grid = (long long)p.n_rtiles * a.B * a.Hkv;
-  attn_tc_kernel<false><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  return a.f16 ? launch_tc<false, true>(tq, tk, tv, p, grid, stream)
+               : launch_tc<false, false>(tq, tk, tv, p, grid, stream);
 }
 
 int tc_split_keys_multiple() { return kN; }
@@ -716,14 +730,14 @@ cudaError_t launch_decode_split_tc(const DecodeSplitArgs& a, const LaunchCtl& ct
     const cuuint64_t dims[3] = {256, cuuint64_t(a.Hq), cuuint64_t(a.T)};
     const cuuint64_t str[2] = {512, cuuint64_t(a.Hq) * 512};
     const cuuint32_t box[3] = {64, cuuint32_t(gqa), cuuint32_t(R)};
-    if (!encode_bf16(fn, &tq, a.Q, 3, dims, str, box)) *encode_failed = true;
+    if (!encode_16b(fn, &tq, a.Q, 3, dims, str, box, a.f16)) *encode_failed = true;
   }
   {
     const cuuint64_t dims[3] = {256, cuuint64_t(a.Lcap), cuuint64_t(a.B) * a.Hkv};
     const cuuint64_t str[2] = {512, cuuint64_t(a.Lcap) * 512};
     const cuuint32_t box[3] = {64, cuuint32_t(kN), 1};
-    if (!encode_bf16(fn, &tk, a.K, 3, dims, str, box)) *encode_failed = true;
-    if (!encode_bf16(fn, &tv, a.V, 3, dims, str, box)) *encode_failed = true;
+    if (!encode_16b(fn, &tk, a.K, 3, dims, str, box, a.f16)) *encode_failed = true;
+    if (!encode_16b(fn, &tv, a.V, 3, dims, str, box, a.f16)) *encode_failed = true;
   }
   if (*encode_failed) return cudaErrorInvalidValue;
 
@@ -747,13 +761,9 @@ cudaError_t launch_decode_split_tc(const DecodeSplitArgs& a, const LaunchCtl& ct
   p.num_splits = a.num_splits;
   p.ctl = ctl;
 
-  const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e != cudaSuccess) return e;
   const long long grid = (long long)a.B * a.Hkv * a.num_splits * p.n_rtiles;
-  attn_tc_kernel<true><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  return a.f16 ? launch_tc<true, true>(tq, tk, tv, p, grid, stream)
+               : launch_tc<true, false>(tq, tk, tv, p, grid, stream);
 }
 
 }  // namespace gqa

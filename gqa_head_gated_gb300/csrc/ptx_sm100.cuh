@@ -152,12 +152,13 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
+// Instruction descriptor, kind::f16 with fp32 D; A and B both bf16 (fmt 1) or both
+// fp16 (fmt 0).
+//   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format,
 //   15 / 16 A / B major (0 = K-major, 1 = MN-major), 17-22 N>>3, 24-28 M>>4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major,
-                                                      int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) |
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn_major, int b_mn_major,
+                                                    uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (uint32_t(a_mn_major) << 15) |
          (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 

@@ -16,7 +16,10 @@
  *
  * Conventions shared by every entry point:
  *   - head_dim D is fixed at 256; every tensor is bf16, contiguous, row-major,
- *     and 16-byte aligned, unless stated otherwise.
+ *     and 16-byte aligned, unless stated otherwise.  Each attention entry point
+ *     has an `_f16` twin (declared at the end) with the same arguments, rules and
+ *     arithmetic whose Q, K, V, G and out are fp16 instead: the d-inference page
+ *     ships FP16 and BF16 symbols of its head_dim-256 kernel.
  *   - Query head h reads KV head h / (Hq / Hkv) (consecutive groups).
  *   - Scores are scaled by 1/16 = 1/sqrt(256).  Softmax sums and all accumulation
  *     are fp32; the output is rounded once to bf16 (round to nearest even).
@@ -24,6 +27,15 @@
  *   - lse outputs, when requested, are fp32 natural-log sum-exp of the scaled
  *     scores over the keys a row sees (-inf for a row that sees no key).
  *   - A row that sees no key outputs zeros.
+ *   - Non-finite inputs: NaN or +-Inf in positions no row of the call sees
+ *     (cache rows at or past kv_len, keys after the last prompt row) never change
+ *     an output, and neither do non-finite K values of keys masked for a row.
+ *     Non-finite Q, G, and K/V of keys that every row of the call sees propagate
+ *     as IEEE float64 arithmetic of the formula would: a NaN score or value gives
+ *     NaN, an Inf value under a positive probability gives +-Inf, a -Inf gate
+ *     gives 0.  A non-finite V row masked for some rows of a call but seen by
+ *     others may turn the masked rows' outputs NaN: they multiply it by
+ *     probability 0 inside the tensor-core product, and 0 * Inf is NaN.
  *   - Ownership: the caller owns every buffer.  The library never allocates
  *     device memory; the decode workspace is caller-provided.
  *   - Streams: every call is asynchronous on `stream` (may be 0 = legacy default
@@ -251,6 +263,38 @@ int gqa_kv_keep(void* Kcache, void* Vcache, const int* kv_lens, const int* cu_ro
  * Read the outcome with gqa_last_device_status().
  */
 int gqa_selftest_wait_timeout(unsigned long long* elapsed_ns, gqa_stream_t stream);
+
+/*
+ * FP16 twins (d-inference PR #640, "Summary": FP16 and BF16 symbols of the
+ * head_dim-256 kernel).  Same arguments, rules, errors and arithmetic as the
+ * bf16 entry point of the same name without `_f16`; Q, K/Kcache, V/Vcache, G and
+ * out are fp16 (IEEE binary16) instead of bf16.  P enters the P.V product as
+ * fp16; the tensor-core kernels rescale a row's running sum whenever its maximum
+ * grows by more than 8 in log2 units, so every P stays at or below 2^8, inside
+ * fp16's range (bf16 uses 32).  Scores, softmax sums and accumulation stay fp32.
+ * Partial results (O_parts, lse_parts) are fp32 in both types.  gqa_kv_append
+ * and gqa_kv_keep copy 16-bit elements and serve both types unchanged.
+ */
+int gqa_attn_prefill_f16(const void* Q, const void* K, const void* V, const void* G, void* out,
+                         float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv, int kv_offset,
+                         gqa_stream_t stream);
+int gqa_attn_decode_f16(const void* Q, const void* Kcache, const void* Vcache, const void* G,
+                        const int* kv_lens, const int* cu_rows, void* out, float* lse_out, int B,
+                        int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
+                        void* workspace, size_t workspace_bytes, gqa_stream_t stream);
+int gqa_attn_verify_tree_f16(const void* Q, const void* Kcache, const void* Vcache,
+                             const void* G, const int* kv_lens, const int* cu_rows,
+                             const unsigned long long* tree_mask, void* out, float* lse_out,
+                             int B, int T, int Hq, int Hkv, int Lcap, int max_rows,
+                             int max_kv_len, void* workspace, size_t workspace_bytes,
+                             gqa_stream_t stream);
+int gqa_attn_decode_split_f16(const void* Q, const void* Kcache, const void* Vcache,
+                              const int* kv_lens, const int* cu_rows, float* O_parts,
+                              float* lse_parts, int B, int T, int Hq, int Hkv, int Lcap,
+                              int max_rows, int max_kv_len, int num_splits, int split_keys,
+                              gqa_stream_t stream);
+int attn_lse_merge_f16(const float* O_parts, const float* lse_parts, int S, int N,
+                       const void* G, void* out, float* lse_out, gqa_stream_t stream);
 
 #ifdef __cplusplus
 }

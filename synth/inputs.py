@@ -8,7 +8,9 @@ Draw order (fixed so that a seed names one input exactly):
   1. structural values (kv lengths, rows per sequence, outlier key positions),
   2. Q, 3. K, 4. V, 5. G,
 each drawn as float32 ``randn`` on a CPU ``torch.Generator`` and rounded to
-bf16 (round to nearest even).  G is ``randn * 2`` (std 2).
+bf16 (round to nearest even), or to fp16 when ``dtype=torch.float16`` (the same
+draws, so a seed names the same real values up to the rounding).  G is
+``randn * 2`` (std 2).
 
 The five named workloads are the head geometries the pages quote for the
 Qwen3.6 family: 24 query heads over 4 KV heads (the 27B) and 16 over 2 (the
@@ -24,8 +26,9 @@ import torch
 HEAD_DIM = 256
 
 
-def _bf16(x: torch.Tensor) -> torch.Tensor:
-    return x.to(torch.bfloat16)
+def _bf16(x: torch.Tensor, dtype=torch.bfloat16) -> torch.Tensor:
+    assert dtype in (torch.bfloat16, torch.float16)
+    return x.to(dtype)
 
 
 @dataclass
@@ -77,7 +80,7 @@ class DecodeInputs:
 
 
 def make_prefill(B, Hq, Hkv, Lq, Lkv=None, kv_offset=0, seed=0, outlier_frac=0.0,
-                 outlier_scale=8.0, g_std=2.0) -> PrefillInputs:
+                 outlier_scale=8.0, g_std=2.0, dtype=torch.bfloat16) -> PrefillInputs:
     """Prompt-row inputs.  ``outlier_frac`` of the key rows of every (b, KV head)
     are multiplied by ``outlier_scale`` (x8 is exact in bf16); positions are drawn
     without replacement before any tensor, one permutation per (b, KV head)."""
@@ -89,20 +92,20 @@ def make_prefill(B, Hq, Hkv, Lq, Lkv=None, kv_offset=0, seed=0, outlier_frac=0.0
     if n_out:
         for _ in range(B * Hkv):
             outliers.append(torch.randperm(Lkv, generator=gen)[:n_out])
-    q = _bf16(torch.randn(B, Hq, Lq, HEAD_DIM, generator=gen))
-    k = _bf16(torch.randn(B, Hkv, Lkv, HEAD_DIM, generator=gen))
-    v = _bf16(torch.randn(B, Hkv, Lkv, HEAD_DIM, generator=gen))
-    g = _bf16(torch.randn(B, Hq, Lq, HEAD_DIM, generator=gen) * g_std)
+    q = _bf16(torch.randn(B, Hq, Lq, HEAD_DIM, generator=gen), dtype)
+    k = _bf16(torch.randn(B, Hkv, Lkv, HEAD_DIM, generator=gen), dtype)
+    v = _bf16(torch.randn(B, Hkv, Lkv, HEAD_DIM, generator=gen), dtype)
+    g = _bf16(torch.randn(B, Hq, Lq, HEAD_DIM, generator=gen) * g_std, dtype)
     if n_out:
         kf = k.view(B * Hkv, Lkv, HEAD_DIM)
         for i, pos in enumerate(outliers):
-            kf[i, pos] = _bf16(kf[i, pos].float() * outlier_scale)
+            kf[i, pos] = _bf16(kf[i, pos].float() * outlier_scale, dtype)
     return PrefillInputs(q, k, v, g, kv_offset, seed,
                          meta=dict(outliers=[p.tolist() for p in outliers]))
 
 
 def make_decode(B, Hq, Hkv, rows, kv_lens, Lcap=None, seed=0, pad_value=float("nan"),
-                g_std=2.0, gen=None) -> DecodeInputs:
+                g_std=2.0, gen=None, dtype=torch.bfloat16) -> DecodeInputs:
     """Decode/verify inputs with explicit rows per sequence and kv lengths.
 
     Keys [0, kv_lens[b]) of every (b, KV head) are drawn; the padding beyond is
@@ -120,15 +123,15 @@ def make_decode(B, Hq, Hkv, rows, kv_lens, Lcap=None, seed=0, pad_value=float("n
     cu = [0]
     for r in rows:
         cu.append(cu[-1] + r)
-    q = _bf16(torch.randn(T, Hq, HEAD_DIM, generator=gen))
+    q = _bf16(torch.randn(T, Hq, HEAD_DIM, generator=gen), dtype)
     fill = 0.0 if pad_value is None else pad_value
-    kc = torch.full((B, Hkv, Lcap, HEAD_DIM), fill, dtype=torch.bfloat16)
-    vc = torch.full((B, Hkv, Lcap, HEAD_DIM), fill, dtype=torch.bfloat16)
+    kc = torch.full((B, Hkv, Lcap, HEAD_DIM), fill, dtype=dtype)
+    vc = torch.full((B, Hkv, Lcap, HEAD_DIM), fill, dtype=dtype)
     for b in range(B):
-        kc[b, :, :kv_lens[b]] = _bf16(torch.randn(Hkv, kv_lens[b], HEAD_DIM, generator=gen))
+        kc[b, :, :kv_lens[b]] = _bf16(torch.randn(Hkv, kv_lens[b], HEAD_DIM, generator=gen), dtype)
     for b in range(B):
-        vc[b, :, :kv_lens[b]] = _bf16(torch.randn(Hkv, kv_lens[b], HEAD_DIM, generator=gen))
-    g = _bf16(torch.randn(T, Hq, HEAD_DIM, generator=gen) * g_std)
+        vc[b, :, :kv_lens[b]] = _bf16(torch.randn(Hkv, kv_lens[b], HEAD_DIM, generator=gen), dtype)
+    g = _bf16(torch.randn(T, Hq, HEAD_DIM, generator=gen) * g_std, dtype)
     return DecodeInputs(q, kc, vc, g, torch.tensor(kv_lens, dtype=torch.int32),
                         torch.tensor(cu, dtype=torch.int32), seed)
 
@@ -152,34 +155,34 @@ def random_tree_masks(rows, seed):
 # The five named workloads.
 # ---------------------------------------------------------------------------
 
-def tiny_prefill():
+def tiny_prefill(dtype=torch.bfloat16):
     """B=1, 24/4 heads, Lq=Lkv=128 causal, seed 0."""
-    return make_prefill(1, 24, 4, 128, seed=0)
+    return make_prefill(1, 24, 4, 128, seed=0, dtype=dtype)
 
 
-def decode_27b(pad_value=float("nan")):
+def decode_27b(pad_value=float("nan"), dtype=torch.bfloat16):
     """B=16 sequences, 24/4 heads, one row each, kv lengths uniform in
     [1024, 32768] in a [16,4,32768,256] cache, seed 1."""
     gen = torch.Generator().manual_seed(1)
     kv = torch.randint(1024, 32769, (16,), generator=gen).tolist()
     return make_decode(16, 24, 4, [1] * 16, kv, Lcap=32768, seed=1, gen=gen,
-                       pad_value=pad_value)
+                       pad_value=pad_value, dtype=dtype)
 
 
-def prefill_27b():
+def prefill_27b(dtype=torch.bfloat16):
     """B=1, 24/4 heads, Lq=Lkv=8192 causal, 1% of key rows x8, seed 2."""
-    return make_prefill(1, 24, 4, 8192, seed=2, outlier_frac=0.01)
+    return make_prefill(1, 24, 4, 8192, seed=2, outlier_frac=0.01, dtype=dtype)
 
 
-def chunked_prefill_35b():
+def chunked_prefill_35b(dtype=torch.bfloat16):
     """B=1, 16/2 heads, a 2048-row chunk at kv_offset 30720 (Lkv 32768), seed 3."""
-    return make_prefill(1, 16, 2, 2048, Lkv=32768, kv_offset=30720, seed=3)
+    return make_prefill(1, 16, 2, 2048, Lkv=32768, kv_offset=30720, seed=3, dtype=dtype)
 
 
 VERIFY_ROWS = (1, 3, 4, 8, 16, 32)
 
 
-def verify_35b(pad_value=float("nan")):
+def verify_35b(pad_value=float("nan"), dtype=torch.bfloat16):
     """B=8, 16/2 heads, rows per sequence from {1,3,4,8,16,32} (taken in turn,
     sequence b gets VERIFY_ROWS[b % 6]), kv lengths uniform in [4097, 65536]
     in a [8,2,65536,256] cache, seed 4."""
@@ -187,7 +190,7 @@ def verify_35b(pad_value=float("nan")):
     kv = torch.randint(4097, 65537, (8,), generator=gen).tolist()
     rows = [VERIFY_ROWS[b % len(VERIFY_ROWS)] for b in range(8)]
     return make_decode(8, 16, 2, rows, kv, Lcap=65536, seed=4, gen=gen,
-                       pad_value=pad_value)
+                       pad_value=pad_value, dtype=dtype)
 
 
 WORKLOADS = {

@@ -43,3 +43,19 @@ def test_prefill_outliers_exact_x8():
         for j in range(200):
             want = k0[g, j] * 8 if j in perms[g] else k0[g, j]
             assert torch.equal(kx[g, j], want)
+
+
+def test_fp16_inputs_are_the_same_draws():
+    """fp16 inputs are the same float32 draws as the bf16 ones, rounded to fp16:
+    the two agree to bf16's rounding (2^-8 relative), and the fp16 values are
+    finer (fp16 keeps 10 mantissa bits)."""
+    a = S.make_decode(2, 4, 2, rows=[2, 1], kv_lens=[5, 3], Lcap=7, seed=9)
+    b = S.make_decode(2, 4, 2, rows=[2, 1], kv_lens=[5, 3], Lcap=7, seed=9, dtype=torch.float16)
+    assert b.q.dtype == torch.float16 and b.k_cache.dtype == torch.float16
+    for x, y in ((a.q, b.q), (a.g, b.g), (a.k_cache[0, :, :5], b.k_cache[0, :, :5])):
+        xf, yf = x.float(), y.float()
+        assert torch.all((xf - yf).abs() <= xf.abs() * 2.0 ** -8 + 1e-30)
+        assert torch.equal(yf.half().float(), yf)
+    assert torch.isnan(b.k_cache[0, :, 5:]).all()
+    p = S.make_prefill(1, 2, 1, 9, seed=3, outlier_frac=0.2, dtype=torch.float16)
+    assert p.q.dtype == torch.float16 and p.k.dtype == torch.float16
