@@ -10,5 +10,5 @@ dropped term, a wrong index or sign, or a transposed operand.
 from .attention import (  # noqa: F401
     HEAD_DIM, SCALE, sigmoid, kv_head_of, prefill_visible, verify_visible,
     attend_rows, prefill, decode, lse_merge, head_chunk_plan, decode_head_chunked,
-    tree_visible_keys, decode_tree, chain_masks, kv_append, kv_keep,
+    tree_visible_keys, decode_tree, chain_masks, kv_append, kv_keep, masked_rows, sdpa_masked,
 )

@@ -331,6 +331,118 @@ def head_chunk_plan(rows: int, gqa: int, enabled: bool = True, limit: int = 32):
     return plan
 
 
+def _broadcast_mask(mask, shape):
+    """The caller's mask as one SDPA call broadcasts it against that call's scores
+    [B, heads, rows, keys] (trailing dimensions aligned, size-1 dimensions
+    repeated).  A mask that cannot broadcast is refused with ValueError."""
+    m = np.asarray(mask)
+    if m.ndim > 4:
+        raise ValueError(f"mask has {m.ndim} dimensions; at most 4")
+    try:
+        return np.broadcast_to(m, shape)
+    except ValueError:
+        raise ValueError(f"mask of shape {m.shape} cannot broadcast to {shape}") from None
+
+
+def masked_rows(q_rows, K, V, g_rows, keep, bias=None):
+    """Gated attention of query rows against one KV head under an explicit mask.
+
+    q_rows [n,D]; K, V [L,D]; g_rows [n,D] or None; keep [n,L] bool (the keys each
+    row attends to); bias [n,L] float64 or None, added to the scaled scores
+    (natural-log units).  Keys a row does not keep are excluded from its sums.  A
+    row that keeps no key outputs zeros and lse -inf.  Returns (out [n,D], lse [n]).
+    """
+    q_rows = np.asarray(q_rows, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    n, D = q_rows.shape
+    out = np.zeros((n, D))
+    lse = np.full(n, -np.inf)
+    for i in range(n):
+        idx = np.nonzero(keep[i])[0]
+        if idx.size == 0:
+            continue
+        s = (K[idx] @ q_rows[i]) * SCALE
+        if bias is not None:
+            s = s + bias[i, idx]
+        m = s.max()
+        p = np.exp(s - m)
+        l = p.sum()
+        o = (p @ V[idx]) / l
+        if g_rows is not None:
+            o = o * sigmoid(np.asarray(g_rows[i], dtype=np.float64))
+        out[i] = o
+        lse[i] = m + np.log(l)
+    return out, lse
+
+
+def sdpa_masked(Q, K, V, G, mask=None, causal=False, kv_offset=None, head_chunking=True):
+    """Gated attention with a general mask, as the DS4Server issue113 README's
+    dense SDPA consumer takes it ("Exact scope found during review"; its fixtures:
+    no, bool, additive, two-dimensional, full-head and chunk-local masks).
+
+    Q, G [B,Hq,Lq,D]; K, V [B,Hkv,Lkv,D].  ``mask``: None, a bool array (True =
+    attend) or a float array (added to the scaled scores; -inf excludes the key
+    like False), of any shape that broadcasts as below.  ``causal``: also exclude
+    keys j > kv_offset + i (kv_offset defaults to Lkv - Lq).
+
+    The head-chunk rule decides how the mask meets the heads: with chunking on,
+    Lq <= 32 and Lq*GQA > 32, every KV group's heads run in chunks of
+    min(GQA, 32 // Lq) (remainder last), each chunk one call that receives the
+    mask unchanged, so the mask must broadcast to [B, chunk, Lq, Lkv] for every
+    chunk, and head k of a chunk reads mask head k (chunk-local).  Otherwise one
+    call takes all Hq heads and the mask must broadcast to [B, Hq, Lq, Lkv].  A
+    mask that cannot broadcast is refused (ValueError) before anything runs.
+    Returns (out [B,Hq,Lq,D], lse [B,Hq,Lq]).
+    """
+    B, Hq, Lq, D = Q.shape
+    Hkv, Lkv = K.shape[1], K.shape[2]
+    assert D == HEAD_DIM and Hq % Hkv == 0
+    gqa = Hq // Hkv
+    if kv_offset is None:
+        kv_offset = Lkv - Lq
+    out = np.zeros((B, Hq, Lq, D))
+    lse = np.full((B, Hq, Lq), -np.inf)
+    if Lq == 0:
+        return out, lse
+    plan = head_chunk_plan(Lq, gqa, head_chunking)
+    # per query head: the [B, Lq, Lkv] slice of the mask its call sees
+    head_mask = [None] * Hq
+    if mask is not None:
+        if len(plan) == 1:
+            M = _broadcast_mask(mask, (B, Hq, Lq, Lkv))
+            for h in range(Hq):
+                head_mask[h] = M[:, h]
+        else:
+            for g in range(Hkv):
+                h0 = g * gqa
+                for c in plan:
+                    M = _broadcast_mask(mask, (B, c, Lq, Lkv))
+                    for k in range(c):
+                        head_mask[h0 + k] = M[:, k]
+                    h0 += c
+    is_bool = mask is not None and np.asarray(mask).dtype == np.bool_
+    base = np.ones((Lq, Lkv), dtype=bool)
+    if causal:
+        base = np.arange(Lkv)[None, :] <= kv_offset + np.arange(Lq)[:, None]
+    for b in range(B):
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            keep, bias = base, None
+            if head_mask[h] is not None:
+                m = head_mask[h][b]
+                if is_bool:
+                    keep = base & m
+                else:
+                    a = np.asarray(m, dtype=np.float64)
+                    keep = base & (a != -np.inf)
+                    bias = np.where(keep, a, 0.0)
+            o, l = masked_rows(Q[b, h], K[b, g], V[b, g], None if G is None else G[b, h],
+                               keep, bias)
+            out[b, h], lse[b, h] = o, l
+    return out, lse
+
+
 def decode_head_chunked(Q, Kc, Vc, G, kv_lens, cu_rows=None, enabled=True):
     """Decode/verify evaluated group by group and head chunk by head chunk, then
     concatenated in head order (DS4Server issue113 README, opening rule).  The

@@ -20,16 +20,19 @@ def _exact(x):
     return Fraction(float(x))
 
 
-def _row(q, keys, vals, gate):
+def _row(q, keys, vals, gate, biases=None):
     """q: list[D] floats; keys/vals: list of rows that the query sees; gate: list[D]
-    or None.  Returns (out list[D] of mpf, lse mpf or None)."""
+    or None; biases: None or one float per key, added exactly to its scaled score.
+    Returns (out list[D] of mpf, lse mpf or None)."""
     D = len(q)
     if not keys:
         return [mpmath.mpf(0)] * D, None
     qf = [_exact(x) for x in q]
     w = []
-    for k in keys:
+    for n, k in enumerate(keys):
         dot = sum((qf[d] * _exact(k[d]) for d in range(D)), Fraction(0)) / 16
+        if biases is not None:
+            dot += _exact(biases[n])
         w.append(mpmath.exp(mpmath.mpf(dot.numerator) / dot.denominator))
     Z = mpmath.fsum(w)
     out = []

@@ -34,6 +34,15 @@ MUTANTS = {
                               "live = [s for s in range(S) if np.isfinite(lse_parts[s, n])]"),
     "sigmoid clamps the gate": ("return 1.0 / (1.0 + np.exp(-x))",
                                 "return 1.0 / (1.0 + np.exp(-np.nan_to_num(x)))"),
+    "mask: bool inverted": ("                    keep = base & m\n", "                    keep = base & ~m\n"),
+    "mask: bias scaled like a score": ("            s = s + bias[i, idx]", "            s = s + bias[i, idx] * SCALE"),
+    "mask: chunk slices the full mask": ("                    M = _broadcast_mask(mask, (B, c, Lq, Lkv))\n",
+                                         "                    M = _broadcast_mask(mask, (B, Hq, Lq, Lkv))[:, h0:h0 + c]\n"),
+    "mask: chunk-local heads reversed": ("                        head_mask[h0 + k] = M[:, k]",
+                                         "                        head_mask[h0 + k] = M[:, c - 1 - k]"),
+    "mask: causal one key too far": ("np.arange(Lkv)[None, :] <= kv_offset + np.arange(Lq)[:, None]",
+                                     "np.arange(Lkv)[None, :] <= kv_offset + 1 + np.arange(Lq)[:, None]"),
+    "mask: -inf bias kept": ("                    keep = base & (a != -np.inf)", "                    keep = base"),
     "scores without NaN": ("s = np.where(seen, s, -np.inf)",
                            "s = np.where(seen & ~np.isnan(s), s, -np.inf)"),
     "merge ignores weights": ("acc += ws * O_parts[s, n]", "acc += O_parts[s, n]"),

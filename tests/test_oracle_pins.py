@@ -18,7 +18,13 @@
   column only, an Inf score poisons exactly the rows whose score is +Inf and
   drops the key where it is -Inf (checked by brute force over the other keys),
   a -Inf gate gives 0, a NaN merge part gives a NaN row, and non-finite values
-  in positions no row sees change nothing.
+  in positions no row sees change nothing;
+* general masks: brute force over the kept keys (bool) and with exact biases
+  (additive), torch's scaled_dot_product_attention with bool and float masks,
+  2-D == expanded 4-D, all-True + causal == prefill, additive -inf == False, a
+  row shift moves only lse, chunk-local == tiled full-head, and the accept /
+  reject table of mask head counts derived from the DS4Server README's rule
+  (tests/golden/mask_head_rules.txt).
 
 Each check is a function returning an error string (empty when it holds) so that
 test_oracle_mutants.py can run the same checks against oracles with planted
@@ -556,6 +562,173 @@ def check_nonfinite_merge(ora):
     return "" if np.isnan(out[2]).all() and np.isnan(lse[2]) else "+Inf lse"
 
 
+# ---------------------------------------------------------------------------
+# general masks (dense SDPA consumer)
+# ---------------------------------------------------------------------------
+
+def _mask_case(seed, B=1, Hq=4, Hkv=2, Lq=3, Lkv=6):
+    x = make_prefill(B, Hq, Hkv, Lq, Lkv=Lkv, kv_offset=Lkv - Lq, seed=seed)
+    return (f64(t) for t in (x.q, x.k, x.v, x.g))
+
+
+def check_masked_brute_bool(ora):
+    """Bool mask (full-head) with the causal rule, against 40-digit brute force
+    over exactly the keys each row keeps; rows keeping nothing are zeros."""
+    Q, K, V, G = _mask_case(60)
+    rng = np.random.default_rng(60)
+    mask = rng.random((1, 4, 3, 6)) < 0.6
+    mask[0, 1, 2] = False                           # a row that keeps no key
+    out, lse = ora.sdpa_masked(Q, K, V, G, mask, causal=True, kv_offset=2,
+                               head_chunking=False)
+    for h in range(4):
+        g = h * 2 // 4
+        for i in range(3):
+            keys = [j for j in range(6) if j <= 2 + i and mask[0, h, i, j]]
+            o, l = brute._row(Q[0, h, i], [K[0, g, j] for j in keys],
+                              [V[0, g, j] for j in keys], G[0, h, i])
+            e = _cmp(out[0, h, i], [float(v) for v in o], 1e-13, f"bool mask row {h, i}")
+            if e:
+                return e
+            if l is None:
+                if lse[0, h, i] != -np.inf or np.any(out[0, h, i] != 0):
+                    return "row with no kept key"
+            elif abs(lse[0, h, i] - float(l)) > 1e-13:
+                return "bool mask lse"
+    return ""
+
+
+def check_masked_brute_additive(ora):
+    """Additive 2-D mask (dyadic values, one -inf) against brute force with the
+    biases added exactly to the scaled scores."""
+    Q, K, V, G = _mask_case(61)
+    rng = np.random.default_rng(61)
+    bias = np.round(rng.normal(0, 2, (3, 6)) * 8) / 8
+    bias[1, 4] = -np.inf
+    out, lse = ora.sdpa_masked(Q, K, V, G, bias)
+    for h in range(4):
+        g = h * 2 // 4
+        for i in range(3):
+            keys = [j for j in range(6) if bias[i, j] != -np.inf]
+            o, l = brute._row(Q[0, h, i], [K[0, g, j] for j in keys],
+                              [V[0, g, j] for j in keys], G[0, h, i],
+                              biases=[bias[i, j] for j in keys])
+            e = _cmp(out[0, h, i], [float(v) for v in o], 1e-13, f"additive row {h, i}")
+            if e or abs(lse[0, h, i] - float(l)) > 1e-13:
+                return e or "additive lse"
+    return ""
+
+
+def check_masked_library_sdpa(ora):
+    """torch scaled_dot_product_attention in float64 (bool and additive attn_mask,
+    GQA by repeat_interleave), ungated, full-head masks without chunking."""
+    import torch.nn.functional as F
+    Q, K, V, _ = _mask_case(62, B=2, Hq=6, Hkv=2, Lq=5, Lkv=9)
+    rng = np.random.default_rng(62)
+    bmask = rng.random((2, 6, 5, 9)) < 0.7
+    bmask[..., 0] = True                            # no fully masked row (torch gives NaN)
+    amask = rng.normal(0, 3, (2, 6, 5, 9))
+    kt = torch.from_numpy(K).repeat_interleave(3, dim=1)
+    vt = torch.from_numpy(V).repeat_interleave(3, dim=1)
+    for m in (bmask, amask):
+        ref = F.scaled_dot_product_attention(torch.from_numpy(Q), kt, vt,
+                                             attn_mask=torch.from_numpy(m), scale=1.0 / 16)
+        out, _ = ora.sdpa_masked(Q, K, V, None, m, head_chunking=False)
+        e = _cmp(out, ref.numpy(), 1e-12, f"library sdpa {m.dtype}")
+        if e:
+            return e
+    return ""
+
+
+def check_masked_reductions(ora):
+    """A 2-D mask equals its explicit 4-D expansion; an all-True mask with the
+    causal rule is the prefill oracle; an additive -inf is a False; adding a
+    constant c to a row's biases keeps its output and moves its lse by c; a row
+    whose biases are all -inf sees no key (zeros, lse -inf)."""
+    Q, K, V, G = _mask_case(63, Lq=4, Lkv=7)
+    rng = np.random.default_rng(63)
+    m2 = rng.random((4, 7)) < 0.6
+    m2[:, 0] = True
+    a, la = ora.sdpa_masked(Q, K, V, G, m2)
+    b, lb = ora.sdpa_masked(Q, K, V, G, np.broadcast_to(m2, (1, 4, 4, 7)).copy())
+    if not (np.array_equal(a, b) and np.array_equal(la, lb)):
+        return "2-D mask differs from its expansion"
+    c, lc = ora.sdpa_masked(Q, K, V, G, np.ones((4, 7), bool), causal=True, kv_offset=3)
+    p, lp = ora.prefill(Q, K, V, G, kv_offset=3)
+    e = _cmp(c, p, 1e-13, "causal all-True") or _cmp(lc, lp, 1e-13, "causal all-True lse")
+    if e:
+        return e
+    add = np.where(m2, 0.0, -np.inf)
+    d, ld = ora.sdpa_masked(Q, K, V, G, add)
+    e = _cmp(d, a, 1e-13, "-inf vs False") or _cmp(ld, la, 1e-13, "-inf vs False lse")
+    if e:
+        return e
+    add2 = add.copy()
+    add2[2] = -np.inf                                 # row 2 excludes every key
+    z, lz = ora.sdpa_masked(Q, K, V, G, add2)
+    if not (np.all(z[:, :, 2] == 0) and np.all(lz[:, :, 2] == -np.inf)):
+        return "a row whose biases are all -inf is not empty"
+    shift = rng.normal(0, 5, (4, 1))
+    f, lf = ora.sdpa_masked(Q, K, V, G, add + shift)
+    return (_cmp(f, a, 1e-12, "row shift") or
+            _cmp(lf, la + shift[:, 0][None, None, :], 1e-12, "row shift lse"))
+
+
+def check_masked_chunk_local(ora):
+    """4 rows x GQA 16 with chunking runs chunks [8, 8]: a chunk-local mask of 8
+    heads gives query head h mask head (h mod 16) mod 8, the same as the tiled
+    full-head mask run without chunking."""
+    Q, K, V, G = _mask_case(64, Hq=32, Hkv=2, Lq=4, Lkv=6)
+    rng = np.random.default_rng(64)
+    local = rng.random((1, 8, 4, 6)) < 0.6
+    local[..., 0] = True
+    full = np.concatenate([local] * 4, axis=1)        # head h -> local[h % 8]
+    a, la = ora.sdpa_masked(Q, K, V, G, local, head_chunking=True)
+    b, lb = ora.sdpa_masked(Q, K, V, G, full, head_chunking=False)
+    if not (np.array_equal(a, b) and np.array_equal(la, lb)):
+        return "chunk-local mask"
+    return ""
+
+
+def _load_mask_rules():
+    rows = []
+    with open(os.path.join(GOLDEN, "mask_head_rules.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].split()
+            if line:
+                r, gqa, hkv, hm = (int(v) for v in line[:4])
+                rows.append((r, gqa, hkv, hm, line[4] == "on", line[5]))
+    return rows
+
+
+def check_mask_rules_golden(ora):
+    """Accept / reject of mask head counts against the rules derived by hand from
+    the page (tests/golden/mask_head_rules.txt), plus refusals of batch, row and
+    key dimensions that do not broadcast and of masks with more than 4 dims."""
+    rules = _load_mask_rules()
+    if len(rules) < 20:
+        return "golden file too short"
+    for r, gqa, hkv, hm, chunking, expect in rules:
+        Q = np.zeros((1, gqa * hkv, r, 256))
+        K = np.zeros((1, hkv, 2, 256))
+        mask = np.ones((1, hm, r, 2), bool)
+        try:
+            ora.sdpa_masked(Q, K, K, None, mask, head_chunking=chunking)
+            got = "ok"
+        except ValueError:
+            got = "reject"
+        if got != expect:
+            return f"rows {r} GQA {gqa} Hkv {hkv} mask heads {hm} chunking {chunking}: {got}"
+    Q = np.zeros((2, 4, 3, 256))
+    K = np.zeros((2, 2, 5, 256))
+    for shape in ((3, 1, 3, 5), (1, 1, 2, 5), (1, 1, 3, 4), (1, 1, 1, 3, 5), (2, 4, 3, 5, 1)):
+        try:
+            ora.sdpa_masked(Q, K, K, None, np.ones(shape, bool), head_chunking=False)
+            return f"mask {shape} accepted"
+        except ValueError:
+            pass
+    return ""
+
+
 CHECKS = [
     check_brute_prefill, check_brute_prefill_ungated, check_brute_decode, check_library_sdpa,
     check_one_key, check_gate_zero_half, check_gate_large_passthrough, check_equal_keys_mean,
@@ -565,6 +738,8 @@ CHECKS = [
     check_tree_storage_permutation, check_kv_append_brute, check_kv_keep_brute,
     check_append_then_chain_verify, check_nonfinite_q_row, check_nonfinite_v_column,
     check_nonfinite_k_sign, check_nonfinite_k_nan, check_nonfinite_gate, check_nonfinite_unseen, check_nonfinite_merge,
+    check_masked_brute_bool, check_masked_brute_additive, check_masked_library_sdpa,
+    check_masked_reductions, check_masked_chunk_local, check_mask_rules_golden,
 ]
 
 
