@@ -19,7 +19,7 @@ from ._lib import GqaError, check, load  # noqa: F401
 
 HEAD_DIM = 256
 
-__all__ = ["prefill", "decode", "verify_tree", "kv_append", "kv_keep", "decode_plan", "decode_split", "lse_merge",
+__all__ = ["prefill", "masked", "decode", "verify_tree", "kv_append", "kv_keep", "decode_plan", "decode_split", "lse_merge",
            "decode_workspace_size", "last_device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "GqaError",
            "load"]
@@ -77,6 +77,59 @@ def prefill(q, k, v, g=None, kv_offset=0, out=None, return_lse=False):
     code = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq, Lkv,
               int(kv_offset), _stream())
     check(code, "gqa_attn_prefill" + sfx)
+    return (out, lse) if return_lse else out
+
+
+_MASK_KIND = {torch.bool: 1, torch.float32: 2, torch.bfloat16: 3, torch.float16: 4}
+
+
+def masked(q, k, v, g=None, mask=None, causal=False, kv_offset=None, head_chunking=True,
+           out=None, return_lse=False):
+    """Gated attention with a general mask (the dense SDPA consumer's masks).
+
+    q, g: [B,Hq,Lq,256]; k, v: [B,Hkv,Lkv,256]; bf16 or fp16.  mask: None, a bool
+    tensor (True = attend) or a float32 / bf16 / fp16 tensor added to the scaled
+    scores, of up to 4 dims broadcasting (trailing dims aligned) to [B, heads, Lq,
+    Lkv]; any strides.  The head rule: with head_chunking, Lq <= 32 and Lq*GQA > 32
+    the mask's head count must be 1 or the chunk size min(GQA, 32 // Lq) with no
+    remainder chunk (chunk-local); otherwise 1 or Hq.  A mask that does not
+    broadcast raises GqaError (GQA_ERR_INVALID_ARG) and launches nothing.
+    causal: also hide keys j > kv_offset + i (kv_offset defaults to Lkv - Lq)."""
+    sfx = _elem(q, "q")
+    _need(q, q.dtype, 4, "q")
+    _need(k, q.dtype, 4, "k")
+    _need(v, q.dtype, 4, "v")
+    if g is not None:
+        _need(g, q.dtype, 4, "g")
+    B, Hq, Lq, _ = q.shape
+    Hkv, Lkv = k.shape[1], k.shape[2]
+    if kv_offset is None:
+        kv_offset = Lkv - Lq
+    kind, mptr = 0, None
+    shape = (ctypes.c_longlong * 4)(1, 1, 1, 1)
+    strides = (ctypes.c_longlong * 4)(0, 0, 0, 0)
+    if mask is not None:
+        if not isinstance(mask, torch.Tensor) or mask.dtype not in _MASK_KIND:
+            raise TypeError("mask must be a bool, float32, bfloat16 or float16 tensor")
+        if not mask.is_cuda:
+            raise ValueError("mask must be a CUDA tensor")
+        if mask.dim() > 4:
+            raise GqaError(1, "gqa_attn_masked: mask has more than 4 dimensions")
+        pad = 4 - mask.dim()
+        for d in range(4):
+            if d >= pad:
+                shape[d] = mask.shape[d - pad]
+                strides[d] = mask.stride(d - pad)
+        kind, mptr = _MASK_KIND[mask.dtype], _ptr(mask)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, q.dtype, 4, "out")
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device) if return_lse else None
+    fn = getattr(load(), "gqa_attn_masked" + sfx)
+    code = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), mptr, kind, shape, strides, _ptr(out),
+              _ptr(lse), B, Hq, Hkv, Lq, Lkv, int(bool(causal)), int(kv_offset),
+              int(bool(head_chunking)), _stream())
+    check(code, "gqa_attn_masked" + sfx)
     return (out, lse) if return_lse else out
 
 

@@ -46,8 +46,11 @@ SIGNATURES = {
                                   _P, ctypes.c_size_t, _P]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      _P]),
+    "gqa_attn_mask_check": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _I]),
+    "gqa_attn_masked": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                             _I, _P]),
 }
-for _name in ("gqa_attn_prefill", "gqa_attn_decode", "gqa_attn_verify_tree",
+for _name in ("gqa_attn_masked", "gqa_attn_prefill", "gqa_attn_decode", "gqa_attn_verify_tree",
               "gqa_attn_decode_split", "attn_lse_merge"):
     SIGNATURES[_name + "_f16"] = SIGNATURES[_name]   # fp16 twins, same arguments
 

@@ -291,6 +291,95 @@ int gqa_attn_verify_tree_impl(bool f16, const void* Q, const void* Kcache, const
   return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
 }
 
+// Which mask head a query head reads (DS4Server issue113 README, "Exact scope found
+// during review": with head chunking the mask goes unchanged to every chunk's call).
+// Chunked when enabled, rows <= 32 and rows * GQA > 32: chunks of min(GQA, 32/rows)
+// heads plus a remainder, and the mask's head count must be 1 or every chunk's size.
+// Otherwise one call over all Hq heads: 1 or Hq.  Returns false for a mask that does
+// not broadcast.
+bool mask_head_mode(int rows, int gqa, int Hq, long long mask_heads, bool chunking, int* mode,
+                    int* chunk) {
+  *chunk = 1;
+  const bool chunked = chunking && rows <= 32 && (long long)rows * gqa > 32;
+  if (mask_heads == 1) {
+    *mode = 0;
+    return true;
+  }
+  if (!chunked) {
+    *mode = 1;
+    return mask_heads == Hq;
+  }
+  const int c = gqa < 32 / rows ? gqa : 32 / rows;
+  if (gqa % c == 0 && mask_heads == c) {
+    *mode = 2;
+    *chunk = c;
+    return true;
+  }
+  return false;
+}
+
+// Host check of a mask description; fills the kernel's head mode and chunk size.
+int check_mask(int B, int Hq, int Hkv, int Lq, int Lkv, int mask_kind,
+               const long long* mask_shape, const long long* mask_strides, int head_chunking,
+               int* hmode, int* chunk) {
+  *hmode = 0;
+  *chunk = 1;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq < 0 || Lkv < 1)
+    return GQA_ERR_INVALID_ARG;
+  if (mask_kind < GQA_MASK_NONE || mask_kind > GQA_MASK_ADD_F16) return GQA_ERR_INVALID_ARG;
+  if (mask_kind == GQA_MASK_NONE) return GQA_OK;
+  if (mask_shape == nullptr || mask_strides == nullptr) return GQA_ERR_INVALID_ARG;
+  const long long want[4] = {B, -1, Lq, Lkv};
+  for (int d = 0; d < 4; ++d) {
+    if (mask_shape[d] < 1 || mask_strides[d] < 0) return GQA_ERR_INVALID_ARG;
+    if (d != 1 && mask_shape[d] != 1 && mask_shape[d] != want[d]) return GQA_ERR_INVALID_ARG;
+  }
+  if (Lq > 0 &&
+      !mask_head_mode(Lq, Hq / Hkv, Hq, mask_shape[1], head_chunking != 0, hmode, chunk))
+    return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
+}
+
+int gqa_attn_masked_impl(bool f16, const void* Q, const void* K, const void* V, const void* G,
+                         const void* mask, int mask_kind, const long long* mask_shape,
+                         const long long* mask_strides, void* out, float* lse_out, int B,
+                         int Hq, int Hkv, int Lq, int Lkv, int causal, int kv_offset,
+                         int head_chunking, gqa_stream_t stream) {
+  PrefillArgs a{Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset};
+  const int st = check_mask(B, Hq, Hkv, Lq, Lkv, mask_kind, mask_shape, mask_strides,
+                            head_chunking, &a.mask_hmode, &a.mask_chunk);
+  if (st != GQA_OK) return st;
+  if (causal != 0 && (kv_offset < 0 || (long long)kv_offset + Lq > Lkv))
+    return GQA_ERR_INVALID_ARG;
+  a.kv_offset = causal != 0 ? kv_offset : 0;
+  a.f16 = f16;
+  a.masked = true;
+  a.causal = causal != 0;
+  a.mask_kind = mask_kind;
+  if (mask_kind != GQA_MASK_NONE) {
+    static const int kElem[5] = {0, 1, 4, 2, 2};
+    if (mask == nullptr || !aligned(mask, size_t(kElem[mask_kind]))) return GQA_ERR_INVALID_ARG;
+    a.mask = mask;
+    for (int d = 0; d < 4; ++d) a.mask_strides[d] = mask_shape[d] == 1 ? 0 : mask_strides[d];
+  }
+  if (Lq == 0) return GQA_OK;
+  if (Q == nullptr || K == nullptr || V == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 16) ||
+      (G != nullptr && !aligned(G, 16)) || (lse_out != nullptr && !aligned(lse_out, 4)))
+    return GQA_ERR_INVALID_ARG;
+  if (Hq / Hkv > 128) return GQA_ERR_UNSUPPORTED;
+  if ((long long)Hq * Lq >= (1LL << 31) || (long long)B * Hkv >= (1LL << 31))
+    return GQA_ERR_UNSUPPORTED;
+  const long long grid = (long long)ceil_div(Lq, prefill_rows_per_tile(Hq / Hkv)) * B * Hkv;
+  if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
+  LaunchCtl ctl;
+  if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
+  bool encode_failed = false;
+  const cudaError_t e = launch_prefill(a, ctl, static_cast<cudaStream_t>(stream), &encode_failed);
+  if (encode_failed) return GQA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
 }  // namespace
 
 }  // namespace gqa
@@ -408,6 +497,32 @@ int gqa_attn_verify_tree_f16(const void* Q, const void* Kcache, const void* Vcac
   return gqa_attn_verify_tree_impl(true, Q, Kcache, Vcache, G, kv_lens, cu_rows, tree_mask, out,
                                    lse_out, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, workspace,
                                    workspace_bytes, stream);
+}
+
+int gqa_attn_mask_check(int B, int Hq, int Hkv, int Lq, int Lkv, int mask_kind,
+                        const long long* mask_shape, const long long* mask_strides,
+                        int head_chunking) {
+  int hmode = 0, chunk = 1;
+  return check_mask(B, Hq, Hkv, Lq, Lkv, mask_kind, mask_shape, mask_strides, head_chunking,
+                    &hmode, &chunk);
+}
+
+int gqa_attn_masked(const void* Q, const void* K, const void* V, const void* G, const void* mask,
+                    int mask_kind, const long long* mask_shape, const long long* mask_strides,
+                    void* out, float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv,
+                    int causal, int kv_offset, int head_chunking, gqa_stream_t stream) {
+  return gqa_attn_masked_impl(false, Q, K, V, G, mask, mask_kind, mask_shape, mask_strides, out,
+                              lse_out, B, Hq, Hkv, Lq, Lkv, causal, kv_offset, head_chunking,
+                              stream);
+}
+int gqa_attn_masked_f16(const void* Q, const void* K, const void* V, const void* G,
+                        const void* mask, int mask_kind, const long long* mask_shape,
+                        const long long* mask_strides, void* out, float* lse_out, int B, int Hq,
+                        int Hkv, int Lq, int Lkv, int causal, int kv_offset, int head_chunking,
+                        gqa_stream_t stream) {
+  return gqa_attn_masked_impl(true, Q, K, V, G, mask, mask_kind, mask_shape, mask_strides, out,
+                              lse_out, B, Hq, Hkv, Lq, Lkv, causal, kv_offset, head_chunking,
+                              stream);
 }
 
 int gqa_last_device_status(gqa_stream_t stream) {

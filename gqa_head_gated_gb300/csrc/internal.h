@@ -18,6 +18,15 @@ struct PrefillArgs {
   float* lse;
   int B, Hq, Hkv, Lq, Lkv, kv_offset;
   bool f16 = false;   // fp16 instead of bf16 elements
+  // General-mask form (gqa_attn_masked).  `masked` selects the kernel that reads a
+  // mask and honours `causal`; the plain prefill is always causal and unmasked.
+  bool masked = false;
+  bool causal = true;
+  const void* mask = nullptr;
+  int mask_kind = 0;        // gqa_mask_kind
+  int mask_hmode = 0;       // 0: one mask head; 1: mask head = query head; 2: chunk-local
+  int mask_chunk = 1;       // chunk size for mode 2
+  long long mask_strides[4] = {0, 0, 0, 0};   // elements; [batch, head, row, key]
 };
 
 // Rows of one prefill tile: floor(128 / GQA) query rows of every head in the group.

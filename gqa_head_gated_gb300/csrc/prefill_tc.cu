@@ -50,6 +50,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include <mutex>
 
 #include "internal.h"
@@ -123,6 +125,10 @@ struct Params {
   float* O_parts;
   float* lse_parts;
   int T, Lcap, max_rows, max_kv_len, split_keys, num_splits;
+  // general-mask prefill (kMask)
+  const void* mask;
+  int mask_kind, mask_hmode, mask_chunk, causal, Lkv;
+  long long ms_b, ms_h, ms_i, ms_j;
   LaunchCtl ctl;
 };
 
@@ -169,7 +175,53 @@ __device__ __forceinline__ void item_kind(int it, int n, bool& is_v, int& j) {
   }
 }
 
-template <bool kSplit, bool kF16>
+// Bias of one mask element in natural-log units: a bool mask gives 0 (attend) or
+// -inf (excluded); an additive mask gives its value.
+__device__ __forceinline__ float mask_bias(uint8_t v) { return v ? 0.f : -INFINITY; }
+__device__ __forceinline__ float mask_bias(float v) { return v; }
+__device__ __forceinline__ float mask_bias(uint16_t v, std::integral_constant<int, 3>) {
+  return __uint_as_float(uint32_t(v) << 16);                       // bf16
+}
+__device__ __forceinline__ float mask_bias(uint16_t v, std::integral_constant<int, 4>) {
+  return __half2float(__ushort_as_half(v));                         // fp16
+}
+
+template <int kKind, typename E>
+__device__ __forceinline__ float mask_elem(E v) {
+  if constexpr (kKind == 3 || kKind == 4)
+    return mask_bias(v, std::integral_constant<int, kKind>{});
+  else
+    return mask_bias(v);
+}
+
+// Applies the mask to one row's raw scores s[0..n) (keys key0 .. key0+n-1, keys at
+// or past `lim` already -inf): an excluded key becomes -inf, a bias a moves the raw
+// score by 16a, so that the scaled score moves by a.  Keys past lim are never read.
+template <int kKind, typename E, int kN_>
+__device__ __forceinline__ void apply_mask_row(uint32_t (&s)[kN_], const E* row, long long sj,
+                                               int key0, int lim) {
+  auto put = [&](int c, float a) {
+    const float v = __uint_as_float(s[c]);
+    s[c] = __float_as_uint(a == -INFINITY ? -INFINITY : fmaf(16.f, a, v));
+  };
+  constexpr int kVec = 16 / int(sizeof(E));
+  const E* m = row + (long long)key0 * sj;
+  if (sj == 1 && key0 + kN_ <= lim && (reinterpret_cast<uintptr_t>(m) & 15) == 0) {
+#pragma unroll
+    for (int c0 = 0; c0 < kN_; c0 += kVec) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(m + c0));
+      const E* e = reinterpret_cast<const E*>(&u);
+#pragma unroll
+      for (int v = 0; v < kVec; ++v) put(c0 + v, mask_elem<kKind>(e[v]));
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < kN_; ++c)
+      if (key0 + c < lim) put(c, mask_elem<kKind>(__ldg(m + (long long)c * sj)));
+  }
+}
+
+template <bool kSplit, bool kF16, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -191,7 +243,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     g = bg % p.Hkv;
     r0 = rt * p.R;
     rows_here = min(p.R, p.Lq - r0);
-    const int n_keys = p.kv_offset + r0 + rows_here;   // keys the last row of the tile sees
+    // keys the last row of the tile sees
+    const int n_keys = (kMask && !p.causal) ? p.Lkv : p.kv_offset + r0 + rows_here;
     n_tiles = (n_keys + kN - 1) / kN;
   } else {
     int bid = static_cast<int>(blockIdx.x);
@@ -418,6 +471,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       rr = row - hh * p.R;
       valid = (row < p.R * p.gqa) && (r0 + rr < p.Lq);
       lim = valid ? p.kv_offset + r0 + rr + 1 : p.kv_offset + r0 + 1;
+      if (kMask && !p.causal) lim = p.Lkv;
     } else {
       rr = row / p.gqa;                   // row m: token r0 + m / GQA, head m % GQA
       hh = row - rr * p.gqa;
@@ -430,6 +484,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int tbase = kSplit && p.tree_mask != nullptr ? kv_len - rows : INT_MAX;
     const int q = r0 + rr;
     const uint32_t trow = tmem + (uint32_t(lq * 32) << 16);
+    // General mask: offset (elements) of this row's mask entries.
+    long long mrow = 0;
+    if constexpr (kMask) {
+      const int mh = p.mask_hmode == 0 ? 0 : p.mask_hmode == 1 ? g * p.gqa + hh
+                                                                 : hh % p.mask_chunk;
+      mrow = (long long)b * p.ms_b + (long long)mh * p.ms_h + (long long)q * p.ms_i;
+    }
 
     float m_run = -INFINITY;
     float l_part = 0.f;
@@ -459,6 +520,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           for (int c = 0; c < kHalf; ++c) {
             const int k = key0 + c - tbase;
             if (k >= 0 && k < 64 && !((tmask >> k) & 1ull)) s[c] = __float_as_uint(-INFINITY);
+          }
+        }
+        if constexpr (kMask) {
+          if (valid && key0 < lim) {
+            switch (p.mask_kind) {
+              case 1:
+                apply_mask_row<1>(s, static_cast<const uint8_t*>(p.mask) + mrow, p.ms_j, key0, lim);
+                break;
+              case 2:
+                apply_mask_row<2>(s, static_cast<const float*>(p.mask) + mrow, p.ms_j, key0, lim);
+                break;
+              case 3:
+                apply_mask_row<3>(s, static_cast<const uint16_t*>(p.mask) + mrow, p.ms_j, key0, lim);
+                break;
+              case 4:
+                apply_mask_row<4>(s, static_cast<const uint16_t*>(p.mask) + mrow, p.ms_j, key0, lim);
+                break;
+              default:
+                break;
+            }
           }
         }
         float m8[8];
@@ -653,14 +734,15 @@ bool encode_16b(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank,
   return r == CUDA_SUCCESS;
 }
 
-template <bool kSplit, bool kF16>
+template <bool kSplit, bool kF16, bool kMask = false>
 cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const Params& p, long long grid, cudaStream_t stream) {
   const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kSplit, kF16>,
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kSplit, kF16, kMask>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<kSplit, kF16><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
+  attn_tc_kernel<kSplit, kF16, kMask>
+      <<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -685,7 +767,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
   }
   {
     // Only keys a row of the call can see are addressable; TMA zero-fills the rest.
-    const cuuint64_t dims[3] = {256, cuuint64_t(a.kv_offset + a.Lq), cuuint64_t(a.B) * a.Hkv};
+    const int kv_hi = a.causal ? a.kv_offset + a.Lq : a.Lkv;
+    const cuuint64_t dims[3] = {256, cuuint64_t(kv_hi), cuuint64_t(a.B) * a.Hkv};
     const cuuint64_t str[2] = {512, cuuint64_t(a.Lkv) * 512};
     const cuuint32_t box[3] = {64, cuuint32_t(kN), 1};   // one column block of a tile
     if (!encode_16b(fn, &tk, a.K, 3, dims, str, box, a.f16)) *encode_failed = true;
@@ -706,8 +789,21 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
   p.R = R;
   p.n_rtiles = (a.Lq + R - 1) / R;
   p.ctl = ctl;
+  p.Lkv = a.Lkv;
+  p.causal = a.causal ? 1 : 0;
+  p.mask = a.mask;
+  p.mask_kind = a.mask_kind;
+  p.mask_hmode = a.mask_hmode;
+  p.mask_chunk = a.mask_chunk;
+  p.ms_b = a.mask_strides[0];
+  p.ms_h = a.mask_strides[1];
+  p.ms_i = a.mask_strides[2];
+  p.ms_j = a.mask_strides[3];
 
   const long long grid = (long long)p.n_rtiles * a.B * a.Hkv;
+  if (a.masked)
+    return a.f16 ? launch_tc<false, true, true>(tq, tk, tv, p, grid, stream)
+                 : launch_tc<false, false, true>(tq, tk, tv, p, grid, stream);
   return a.f16 ? launch_tc<false, true>(tq, tk, tv, p, grid, stream)
                : launch_tc<false, false>(tq, tk, tv, p, grid, stream);
 }

@@ -265,6 +265,56 @@ int gqa_kv_keep(void* Kcache, void* Vcache, const int* kv_lens, const int* cu_ro
 int gqa_selftest_wait_timeout(unsigned long long* elapsed_ns, gqa_stream_t stream);
 
 /*
+ * Gated attention with a general mask: the dense SDPA consumer of the DS4Server
+ * issue113 README ("Exact scope found during review"; its fixtures cover no,
+ * bool, additive, two-dimensional, full-head and chunk-local masks, and mask
+ * rejections), in the prefill layout:
+ *   Q, G, out: [B, Hq, Lq, 256]; K, V: [B, Hkv, Lkv, 256]; bf16 (fp16: _f16).
+ *   score(i, j) = Q_i . K_j / 16 + bias(i, j); a key is excluded when a bool mask
+ *   holds 0 there, when an additive mask holds -inf, or (causal != 0) when
+ *   j > kv_offset + i.  A row that keeps no key outputs zeros, lse -inf.
+ * mask: NULL with mask_kind GQA_MASK_NONE (then only the causal rule, or none), or
+ *   a device array read at  mask[b*s0 + hm*s1 + i*s2 + j*s3]  with mask_shape /
+ *   mask_strides (host arrays of 4, elements, order [batch, head, row, key]); a
+ *   dimension of size 1 broadcasts (its stride is ignored); otherwise batch must
+ *   be B, row Lq, key Lkv.  Strides >= 0; the pointer aligned to its element.
+ *   GQA_MASK_BOOL: uint8, nonzero = attend.  GQA_MASK_ADD_F32 / _BF16 / _F16: a
+ *   value added to the scaled score (natural-log units).
+ * Head rule (head_chunking != 0 is the page's default): when Lq <= 32 and
+ *   Lq * GQA > 32, each KV group's heads run in chunks of min(GQA, 32 / Lq) heads
+ *   (a smaller remainder last) and the mask is passed unchanged to every chunk,
+ *   so its head count must be 1 or equal to every chunk's size, and query head
+ *   k of a chunk reads mask head k (chunk-local).  Otherwise (or head_chunking
+ *   == 0) the head count must be 1 or Hq and query head h reads mask head h.
+ *   A mask that does not broadcast returns GQA_ERR_INVALID_ARG, launching
+ *   nothing.  Head chunking changes no value: only which masks are accepted.
+ * causal: 0 = every key of Lkv may be seen; 1 = also j <= kv_offset + i (then
+ *   0 <= kv_offset, kv_offset + Lq <= Lkv).  Runs on the tcgen05 prefill kernel.
+ */
+typedef enum {
+  GQA_MASK_NONE = 0,
+  GQA_MASK_BOOL = 1,
+  GQA_MASK_ADD_F32 = 2,
+  GQA_MASK_ADD_BF16 = 3,
+  GQA_MASK_ADD_F16 = 4
+} gqa_mask_kind;
+
+int gqa_attn_masked(const void* Q, const void* K, const void* V, const void* G, const void* mask,
+                    int mask_kind, const long long* mask_shape, const long long* mask_strides,
+                    void* out, float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv,
+                    int causal, int kv_offset, int head_chunking, gqa_stream_t stream);
+
+/*
+ * Host-only check of a mask description against gqa_attn_masked's rules (sizes,
+ * kind, broadcast of batch / row / key dimensions, strides >= 0, the head rule);
+ * GQA_OK or GQA_ERR_INVALID_ARG.  Makes no CUDA call.  gqa_attn_masked runs the
+ * same check first.
+ */
+int gqa_attn_mask_check(int B, int Hq, int Hkv, int Lq, int Lkv, int mask_kind,
+                        const long long* mask_shape, const long long* mask_strides,
+                        int head_chunking);
+
+/*
  * FP16 twins (d-inference PR #640, "Summary": FP16 and BF16 symbols of the
  * head_dim-256 kernel).  Same arguments, rules, errors and arithmetic as the
  * bf16 entry point of the same name without `_f16`; Q, K/Kcache, V/Vcache, G and
@@ -295,6 +345,11 @@ int gqa_attn_decode_split_f16(const void* Q, const void* Kcache, const void* Vca
                               gqa_stream_t stream);
 int attn_lse_merge_f16(const float* O_parts, const float* lse_parts, int S, int N,
                        const void* G, void* out, float* lse_out, gqa_stream_t stream);
+int gqa_attn_masked_f16(const void* Q, const void* K, const void* V, const void* G,
+                        const void* mask, int mask_kind, const long long* mask_shape,
+                        const long long* mask_strides, void* out, float* lse_out, int B, int Hq,
+                        int Hkv, int Lq, int Lkv, int causal, int kv_offset, int head_chunking,
+                        gqa_stream_t stream);
 
 #ifdef __cplusplus
 }

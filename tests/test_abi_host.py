@@ -171,3 +171,49 @@ def test_kv_append_keep_reject_before_launch(lib):
     assert k(P(16), P(32), P(48), P(64), P(80), P(96), P(48), 2, 2, 10, None) == 1  # out aliases in
     assert k(P(16), P(32), P(48), None, P(80), P(96), None, 2, 2, 10, None) == 1
     assert k(P(16), P(32), P(48), P(64), P(80), P(96), None, 0, 2, 10, None) == 1
+
+
+def _mask_rules():
+    path = os.path.join(ROOT, "tests", "golden", "mask_head_rules.txt")
+    rows = []
+    for line in open(path):
+        f = line.split("#")[0].split()
+        if f:
+            rows.append((int(f[0]), int(f[1]), int(f[2]), int(f[3]), f[4] == "on", f[5]))
+    return rows
+
+
+def test_mask_check_matches_the_head_rule_table(lib):
+    """gqa_attn_mask_check (host only) accepts and refuses mask head counts exactly as
+    the table derived from the DS4Server README's rule says; batch, row and key
+    dimensions must be 1 or the call's size; strides must be >= 0; kinds 0..4."""
+    LL4 = ctypes.c_longlong * 4
+    for rows, gqa, hkv, hm, chunking, expect in _mask_rules():
+        code = lib.gqa_attn_mask_check(1, gqa * hkv, hkv, rows, 2, 1, LL4(1, hm, rows, 2),
+                                       LL4(0, rows * 2, 2, 1), int(chunking))
+        assert code == (0 if expect == "ok" else 1), (rows, gqa, hkv, hm, chunking)
+    chk = lambda shape, strides=(0, 0, 0, 1), kind=1: lib.gqa_attn_mask_check(
+        2, 4, 2, 3, 5, kind, LL4(*shape), LL4(*strides), 1)
+    assert chk((2, 4, 3, 5)) == 0 and chk((1, 1, 1, 1)) == 0 and chk((1, 1, 3, 1)) == 0
+    assert chk((3, 1, 3, 5)) == 1 and chk((1, 1, 2, 5)) == 1 and chk((1, 1, 3, 4)) == 1
+    assert chk((1, 2, 3, 5)) == 1 and chk((0, 1, 3, 5)) == 1
+    assert chk((1, 1, 3, 5), strides=(0, 0, -5, 1)) == 1
+    assert chk((1, 1, 3, 5), kind=5) == 1 and chk((1, 1, 3, 5), kind=-1) == 1
+    assert lib.gqa_attn_mask_check(2, 4, 2, 3, 5, 0, None, None, 1) == 0     # no mask
+    assert lib.gqa_attn_mask_check(2, 4, 2, 3, 5, 1, None, None, 1) == 1
+
+
+def test_masked_rejects_before_launch(lib):
+    """gqa_attn_masked refuses bad masks, a missing mask pointer, a misaligned
+    additive mask and a causal offset past the keys, before any CUDA call."""
+    LL4 = ctypes.c_longlong * 4
+    f = lib.gqa_attn_masked
+    def call(mask=64, kind=1, shape=(1, 1, 3, 5), causal=0, off=0, Lq=3):
+        return f(P(16), P(32), P(48), None, P(mask) if mask else None, kind, LL4(*shape),
+                 LL4(0, 0, 5, 1), P(80), None, 1, 4, 2, Lq, 5, causal, off, 1, None)
+    assert call(shape=(1, 3, 3, 5)) == 1
+    assert call(mask=None) == 1
+    assert call(mask=66, kind=2) == 1             # fp32 mask not 4-byte aligned
+    assert call(causal=1, off=3) == 1             # 3 + 3 rows > 5 keys
+    assert call(kind=7) == 1
+    assert call(Lq=0, shape=(1, 1, 1, 5)) == 0    # nothing to do
