@@ -570,6 +570,48 @@ def ours(args):
             "peak_note": "fp16 dense peak = measured bf16 burst peak x 1 (equal nominal rates)",
             "avg_ms": round(pff_avg, 4)}
         del pff
+        # General masks on the 27B prefill (gqa_attn_masked, causal rule on): an additive
+        # bf16 bias [8192, 8192] broadcast over batch and heads (every causal pair stays
+        # visible, so the FLOPs equal the plain prefill's), and a bool block-diagonal
+        # document mask (documents of 1024 rows)
+        q_, k_, v_, g_ = (t.to(dev) for t in (pf.q, pf.k, pf.v, pf.g))
+        Lp = q_.shape[2]
+        gen = torch.Generator().manual_seed(7)
+        bias = (torch.randn(Lp, Lp, generator=gen) * 2).to(torch.bfloat16).to(dev)
+        doc = torch.arange(Lp, device=dev) // 1024
+        docm = doc[:, None] == doc[None, :]
+        mout = torch.empty_like(q_)
+        for name, m in (("masked_prefill_27b_bias", bias), ("masked_prefill_27b_doc", docm)):
+            for _ in range(max(3, args.warmup)):
+                ctx["flush"]()
+                G.masked(q_, k_, v_, g_, m, causal=True, kv_offset=0, out=mout)
+            torch.cuda.synchronize()
+            mp = []
+            for _ in range(pf_steps):
+                ctx["flush"]()
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record()
+                G.masked(q_, k_, v_, g_, m, causal=True, kv_offset=0, out=mout)
+                b_.record()
+                mp.append((a_, b_))
+            torch.cuda.synchronize()
+            m_avg = sum(a_.elapsed_time(b_) for a_, b_ in mp) / len(mp)
+            entry = {"value": round(flops / (m_avg / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                     "frac_of_bf16_peak": round(flops / (m_avg / 1e3) / 1e12 / bf16_peak, 4),
+                     "avg_ms": round(m_avg, 4), "vs_unmasked_prefill": round(pf_avg / m_avg, 4),
+                     "mask_bytes": m.numel() * m.element_size()}
+            if name.endswith("bias"):
+                entry["workload"] = ("the 27B prefill with an additive bf16 bias [8192, 8192] "
+                                     "(N(0,2), seed 7) broadcast over heads, causal")
+            else:
+                vis = 8 * (1024 * 1025 // 2)
+                entry["workload"] = ("the 27B prefill with a bool block-diagonal document mask "
+                                     "(8 documents of 1024 rows), causal; value counts every "
+                                     "causal pair the kernel computes")
+                entry["visible_pair_tflops"] = round(4.0 * 256 * vis * 24 / (m_avg / 1e3) / 1e12, 2)
+            more[name] = entry
+        del q_, k_, v_, g_, bias, docm, mout
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0:
