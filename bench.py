@@ -283,28 +283,30 @@ def setup_decode(x, steps, dev, with_rows=False):
     T, Hq = q.shape[0], q.shape[1]
     max_kv = int(x.kv_lens.max())
     S_, C_ = G.decode_plan(B, T, Hq, Hkv, max_rows, max_kv)
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(steps)]
+    ws = torch.empty(G.decode_workspace_size(B, T, Hq, Hkv, max_rows, max_kv), dtype=torch.uint8,
+                     device=dev)
     return dict(q=q, kc=kc, vc=vc, g=g, kv=kv, cu=cu, max_rows=max_rows, max_kv=max_kv,
-                plan=(S_, C_), ev=ev,
-                op=torch.empty((S_, T * Hq, 256), dtype=torch.float32, device=dev),
-                lp=torch.empty((S_, T * Hq), dtype=torch.float32, device=dev),
-                out=torch.empty_like(q), flush=L2Flush(dev))
+                plan=(S_, C_), ev=ev, ws=ws, out=torch.empty_like(q), flush=L2Flush(dev))
 
 
-def run_decode_timed(ctx, steps):
-    """One decode step = the split kernel then the merge (both through the C ABI), each
-    bracketed by events on the launching (current) stream; L2 flushed before each."""
+def run_decode_timed(ctx, steps, tree_mask=None):
+    """One decode step = one gqa_attn_decode call (gqa_attn_verify_tree with a tree
+    mask): a counter memset and the split kernel whose last CTA per row group merges
+    the group's partial results (fused merge).  Bracketed by events on the launching
+    (current) stream; L2 flushed before each step, outside the events."""
     import gqa_head_gated_gb300 as G
-    q, kc, vc, kv = ctx["q"], ctx["kc"], ctx["vc"], ctx["kv"]
-    S_, C_ = ctx["plan"]
+    q, kc, vc, kv, g = ctx["q"], ctx["kc"], ctx["vc"], ctx["kv"], ctx["g"]
     for i in range(steps):
         ctx["flush"]()
-        a, m, b = ctx["ev"][i % len(ctx["ev"])]
+        a, b = ctx["ev"][i % len(ctx["ev"])]
         a.record()
-        G.decode_split(q, kc, vc, kv, ctx["cu"], max_rows=ctx["max_rows"], max_kv_len=ctx["max_kv"],
-                       num_splits=S_, split_keys=C_, o_parts=ctx["op"], lse_parts=ctx["lp"])
-        m.record()
-        G.lse_merge(ctx["op"], ctx["lp"], ctx["g"], out=ctx["out"].view(-1, 256))
+        if tree_mask is None:
+            G.decode(q, kc, vc, g, kv, ctx["cu"], max_rows=ctx["max_rows"],
+                     max_kv_len=ctx["max_kv"], workspace=ctx["ws"], out=ctx["out"])
+        else:
+            G.verify_tree(q, kc, vc, g, kv, ctx["cu"], tree_mask, max_rows=ctx["max_rows"],
+                          max_kv_len=ctx["max_kv"], workspace=ctx["ws"], out=ctx["out"])
         b.record()
 
 
@@ -416,10 +418,26 @@ def ours(args):
         run_decode_timed(ctx, args.steps)
         torch.cuda.synchronize()
     barrier(world)
-    split_ms = [a.elapsed_time(m) for a, m, b in ctx["ev"]]
-    merge_ms = [m.elapsed_time(b) for a, m, b in ctx["ev"]]
-    total_ms = sum(a.elapsed_time(b) for a, m, b in ctx["ev"])
-    total_ms = max_over_ranks(world, total_ms)
+    step_ms = [a.elapsed_time(b) for a, b in ctx["ev"]]
+    total_ms = max_over_ranks(world, sum(step_ms))
+    # The dominant kernel alone (for the roofline): the same split launch, K more steps,
+    # events around gqa_attn_decode_split on the same stream, L2 flushed before each.
+    T_, Hq_ = x.q.shape[:2]
+    op = torch.empty((S_, T_ * Hq_, 256), dtype=torch.float32, device=dev)
+    lp = torch.empty((S_, T_ * Hq_), dtype=torch.float32, device=dev)
+    split_ms = []
+    for i in range(args.warmup + args.steps):
+        ctx["flush"]()
+        a, b = ctx["ev"][i % len(ctx["ev"])]
+        a.record()
+        G.decode_split(ctx["q"], ctx["kc"], ctx["vc"], ctx["kv"], None, max_rows=1,
+                       max_kv_len=ctx["max_kv"], num_splits=S_, split_keys=C_, o_parts=op,
+                       lse_parts=lp)
+        b.record()
+        b.synchronize()
+        if i >= args.warmup:
+            split_ms.append(a.elapsed_time(b))
+    del op, lp
     status = G.last_device_status()
     out_ok = bool(torch.isfinite(ctx["out"].float()).all().item())
 
@@ -465,51 +483,28 @@ def ours(args):
         torch.cuda.synchronize()
         run_decode_timed(vctx, args.steps)
         torch.cuda.synchronize()
-        v_split = sum(a.elapsed_time(m) for a, m, b in vctx["ev"]) / args.steps
-        v_step = sum(a.elapsed_time(b) for a, m, b in vctx["ev"]) / args.steps
+        v_step = sum(a.elapsed_time(b) for a, b in vctx["ev"]) / args.steps
         more["verify_35b"] = {
             "workload": "35B-A3B draft verify: B=8, Hq=16, Hkv=2, rows [1,3,4,8,16,32,1,3], "
                         "kv_lens 4271..45513 in a [8,2,65536,256] cache, seed 4",
             "value": round(v_bytes / (v_step / 1e3) / 1e9, 2), "unit": "GB/s",
             "frac_of_hbm": round(v_bytes / (v_step / 1e3) / 1e9 / hbm_peak, 4),
-            "split_kernel_gbs": round((v_kv + vx.q.numel() * 2) / (v_split / 1e3) / 1e9, 2),
             "split_plan": {"num_splits": vctx["plan"][0], "split_keys": vctx["plan"][1]},
             "ms_per_step": round(v_step, 5)}
         # the same verify workload over seeded token trees (one 64-bit mask per row)
-        import gqa_head_gated_gb300 as G
         tm = torch.tensor(S.random_tree_masks(vx.rows, 5), dtype=torch.int64, device=dev)
-        Bv, Hkvv = vx.k_cache.shape[:2]
-        Tv, Hqv = vx.q.shape[:2]
-        ws = torch.empty(G.decode_workspace_size(Bv, Tv, Hqv, Hkvv, max(vx.rows),
-                                                 vctx["max_kv"]), dtype=torch.uint8, device=dev)
-        tout = torch.empty_like(vctx["q"])
-        cud = vx.cu_rows.to(dev)
-
-        def tree_step():
-            G.verify_tree(vctx["q"], vctx["kc"], vctx["vc"], vctx["g"], vctx["kv"], cud, tm,
-                          max_rows=max(vx.rows), max_kv_len=vctx["max_kv"], workspace=ws,
-                          out=tout)
-        for _ in range(args.warmup):
-            vctx["flush"]()
-            tree_step()
+        run_decode_timed(vctx, args.warmup, tree_mask=tm)
         torch.cuda.synchronize()
-        tms = []
-        for _ in range(args.steps):
-            vctx["flush"]()
-            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a_.record()
-            tree_step()
-            b_.record()
-            tms.append((a_, b_))
+        run_decode_timed(vctx, args.steps, tree_mask=tm)
         torch.cuda.synchronize()
-        t_avg = sum(a_.elapsed_time(b_) for a_, b_ in tms) / len(tms)
+        t_avg = sum(a.elapsed_time(b) for a, b in vctx["ev"]) / args.steps
         more["verify_tree_35b"] = {
             "workload": "the 35B draft-verify workload over seeded token trees "
                         "(synth.random_tree_masks(rows, 5)), gqa_attn_verify_tree",
             "value": round(v_bytes / (t_avg / 1e3) / 1e9, 2), "unit": "GB/s",
             "frac_of_hbm": round(v_bytes / (t_avg / 1e3) / 1e9 / hbm_peak, 4),
             "ms_per_step": round(t_avg, 5)}
-        del vctx, vx, ws, tout
+        del vctx, vx
         torch.cuda.empty_cache()
         # KV-cache append of a whole 8192-row prompt's K/V (24/4 heads) into a cache
         kn = pf.k.to(dev)[0].transpose(0, 1).contiguous()      # [8192, 4, 256]
@@ -548,15 +543,12 @@ def ours(args):
         torch.cuda.synchronize()
         run_decode_timed(fctx, args.steps)
         torch.cuda.synchronize()
-        f_split = sum(a.elapsed_time(m) for a, m, b in fctx["ev"]) / args.steps
-        f_step = sum(a.elapsed_time(b) for a, m, b in fctx["ev"]) / args.steps
+        f_step = sum(a.elapsed_time(b) for a, b in fctx["ev"]) / args.steps
         f_ok = bool(torch.isfinite(fctx["out"].float()).all().item())
         more["decode_27b_fp16"] = {
-            "workload": "the 27B-shape decode workload in fp16 (gqa_attn_decode_split_f16 + "
-                        "attn_lse_merge_f16)",
+            "workload": "the 27B-shape decode workload in fp16 (gqa_attn_decode_f16)",
             "value": round(step_bytes / (f_step / 1e3) / 1e9, 2), "unit": "GB/s",
             "frac_of_hbm": round(step_bytes / (f_step / 1e3) / 1e9 / hbm_peak, 4),
-            "split_kernel_gbs": round(split_bytes / (f_split / 1e3) / 1e9, 2),
             "ms_per_step": round(f_step, 5), "outputs_finite": f_ok}
         del fctx, xf
         torch.cuda.empty_cache()
@@ -655,9 +647,14 @@ def ours(args):
                 "traffic": args.traffic if args.traffic is not None else
                 dram_traffic("decode_split_kernel", int(x.kv_lens.sum()) * x.k_cache.shape[1]),
                 "avg_launch_ms": round(split_avg, 5),
+                "timing": "events around gqa_attn_decode_split alone (same plan and inputs), "
+                          "K steps right after the headline steps, L2 flushed before each",
                 "algorithmic_bytes_per_launch": split_bytes,
             },
-            "merge_avg_ms": round(sum(merge_ms) / len(merge_ms), 5),
+            "step_note": "one gqa_attn_decode call per step: decode_split_kernel, then "
+                         "lse_merge_kernel launched as its programmatic dependent (scheduled "
+                         "while the split kernel drains; it waits for the split grid before "
+                         "reading the parts)",
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "note": "gqa_attn_decode with pinned host Q/G/kv_lens in and out back; "

@@ -217,7 +217,8 @@ int gqa_attn_decode_split_impl(bool f16, const void* Q, const void* Kcache, cons
 }
 
 int attn_lse_merge_impl(bool f16, const float* O_parts, const float* lse_parts, int S, int N,
-                        const void* G, void* out, float* lse_out, gqa_stream_t stream) {
+                        const void* G, void* out, float* lse_out, gqa_stream_t stream,
+                        bool after_split = false) {
   if (S < 1 || N < 0) return GQA_ERR_INVALID_ARG;
   if (N == 0) return GQA_OK;
   if (O_parts == nullptr || lse_parts == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
@@ -228,6 +229,7 @@ int attn_lse_merge_impl(bool f16, const float* O_parts, const float* lse_parts, 
   if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
   MergeArgs a{O_parts, lse_parts, S, N, G, out, lse_out};
   a.f16 = f16;
+  a.after_split = after_split;
   return launch_lse_merge(a, ctl, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_CUDA;
@@ -258,7 +260,8 @@ int gqa_attn_decode_impl(bool f16, const void* Q, const void* Kcache, const void
                                      lse_parts, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, S, C,
                                      stream);
   if (r != GQA_OK) return r;
-  return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
+  return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream,
+                             true);
 }
 
 int gqa_attn_verify_tree_impl(bool f16, const void* Q, const void* Kcache, const void* Vcache,
@@ -288,7 +291,8 @@ int gqa_attn_verify_tree_impl(bool f16, const void* Q, const void* Kcache, const
   int r = run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
                     max_rows, max_kv_len, S, C, static_cast<cudaStream_t>(stream), tree_mask, f16);
   if (r != GQA_OK) return r;
-  return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream);
+  return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream,
+                             true);
 }
 
 // Which mask head a query head reads (DS4Server issue113 README, "Exact scope found

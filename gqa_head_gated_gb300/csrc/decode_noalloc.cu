@@ -85,6 +85,7 @@ int gqa_attn_decode_noalloc(const void* Q, const void* Kcache, const void* Vcach
                     Lcap, max_rows, max_kv_len, S, C};
   if (launch_decode_split(a, ctl, s) != cudaSuccess) return GQA_ERR_CUDA;
   MergeArgs m{O_parts, lse_parts, S, T * Hq, G, out, lse_out};
+  m.after_split = true;
   return launch_lse_merge(m, ctl, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 

@@ -125,6 +125,9 @@ decode_split_kernel(const Params p) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // The merge launched after this kernel (programmatic dependent launch) may be
+  // scheduled once every CTA has started; it still waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;");
 
   int bid = blockIdx.x;
   const int rb = bid % p.n_rb;

@@ -73,6 +73,9 @@ struct MergeArgs {
   void* out;
   float* lse_out;
   bool f16 = false;   // fp16 instead of bf16 G / out
+  // Launched right after the library's split kernel on the same stream: programmatic
+  // dependent launch (the merge is scheduled while the split kernel drains).
+  bool after_split = false;
 };
 
 cudaError_t launch_lse_merge(const MergeArgs& a, const LaunchCtl& ctl, cudaStream_t stream);

@@ -10,7 +10,10 @@
 // dropping later tail chunks" must fail).  Parts with lse = -inf carry weight 0
 // and their O rows are never read.  A NaN lse (a part that saw a NaN score)
 // makes the row NaN, as float64 arithmetic of the formula would.  One warp per
-// row; each lane owns 8 of the 256 columns and reads them as two float4 per part.
+// row; each lane owns 8 of the 256 columns and reads them as two float4 per part,
+// the loads of eight parts issued together (the kernel is latency-bound: a decode
+// merge moves a few MB).  It is launched as a programmatic dependent of the split
+// kernel, so its launch overlaps that kernel's last CTAs.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,66 +24,29 @@ namespace {
 
 constexpr int kWarps = 8;
 
+// Waits (hardware dependency, no spinning) until the kernel this launch depends on
+// programmatically has completed and its writes are visible; returns at once when
+// there is no such kernel.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+constexpr int kBatch = 8;   // parts whose loads are issued together
+
 template <bool kF16>
 __global__ void __launch_bounds__(kWarps * 32)
 lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ lse_parts, int S,
                  int N, const uint16_t* __restrict__ G, uint16_t* __restrict__ out,
-                 float* __restrict__ lse_out) {
+                 float* __restrict__ lse_out, int gate_early) {
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (n >= N) return;
   const size_t stride = size_t(N);
-
-  // Max over parts, 32 parts per round (lane s reads part s of the round).  fmaxf
-  // drops NaN; a NaN part still gets weight NaN below.
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse_parts + size_t(s) * stride + n));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
   const int c0 = lane * 8;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float wsum = 0.f;
-  const float Msub = M == -INFINITY ? 0.f : M;
-  {
-    for (int s0 = 0; s0 < S; s0 += 32) {
-      // lane s holds the weight of part s0 + s (0 for an empty or missing part)
-      const int sl = s0 + lane;
-      const float ls = sl < S ? __ldg(lse_parts + size_t(sl) * stride + n) : -INFINITY;
-      const float wl = ls == -INFINITY ? 0.f : __expf(ls - Msub);
-      const int cnt = min(32, S - s0);
-      // Batches of 4 parts: the loads of a batch are issued together.
-      for (int b = 0; b < cnt; b += 4) {
-        float w[4];
-        float4 va[4], vb[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          w[u] = __shfl_sync(0xffffffffu, wl, min(b + u, 31));
-          if (b + u >= cnt) w[u] = 0.f;
-          va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (w[u] != 0.f) {
-            const float4* src = reinterpret_cast<const float4*>(
-                O_parts + (size_t(s0 + b + u) * stride + n) * 256 + c0);
-            va[u] = __ldg(src);
-            vb[u] = __ldg(src + 1);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          wsum += w[u];
-          acc[0] += w[u] * va[u].x;
-          acc[1] += w[u] * va[u].y;
-          acc[2] += w[u] * va[u].z;
-          acc[3] += w[u] * va[u].w;
-          acc[4] += w[u] * vb[u].x;
-          acc[5] += w[u] * vb[u].y;
-          acc[6] += w[u] * vb[u].z;
-          acc[7] += w[u] * vb[u].w;
-        }
-      }
-    }
-  }
-  const float inv = wsum == 0.f ? 0.f : 1.f / wsum;
+
+  // After the library's own split kernel the gate, written before that kernel in
+  // stream order, is read before waiting for it (gate_early); otherwise after.
+  if (!gate_early) grid_dependency_wait();
   float gs[8];
   if (G != nullptr) {
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(G + size_t(n) * 256 + c0));
@@ -95,6 +61,56 @@ lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ ls
 #pragma unroll
     for (int e = 0; e < 8; ++e) gs[e] = 1.f;
   }
+  if (gate_early) grid_dependency_wait();
+
+  // Max over parts (lane s reads part s of each round of 32).  fmaxf drops NaN; a NaN
+  // part still gets weight NaN below.  With S <= 32 the first round's values are kept.
+  const float ls0 = lane < S ? __ldcg(lse_parts + size_t(lane) * stride + n) : -INFINITY;
+  float M = ls0;
+  for (int s = lane + 32; s < S; s += 32) M = fmaxf(M, __ldcg(lse_parts + size_t(s) * stride + n));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+  const float Msub = M == -INFINITY ? 0.f : M;
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    // lane s holds the weight of part s0 + s (0 for an empty or missing part)
+    const int sl = s0 + lane;
+    const float ls = s0 == 0 ? ls0 : sl < S ? __ldcg(lse_parts + size_t(sl) * stride + n)
+                                            : -INFINITY;
+    const float wl = ls == -INFINITY ? 0.f : __expf(ls - Msub);
+    const int cnt = min(32, S - s0);
+    for (int b = 0; b < cnt; b += kBatch) {
+      float w[kBatch];
+      float4 va[kBatch], vb[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        w[u] = __shfl_sync(0xffffffffu, wl, min(b + u, 31));
+        if (b + u >= cnt) w[u] = 0.f;
+        va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (w[u] != 0.f) {
+          const float4* src = reinterpret_cast<const float4*>(
+              O_parts + (size_t(s0 + b + u) * stride + n) * 256 + c0);
+          va[u] = __ldcg(src);
+          vb[u] = __ldcg(src + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        wsum += w[u];
+        acc[0] += w[u] * va[u].x;
+        acc[1] += w[u] * va[u].y;
+        acc[2] += w[u] * va[u].z;
+        acc[3] += w[u] * va[u].w;
+        acc[4] += w[u] * vb[u].x;
+        acc[5] += w[u] * vb[u].y;
+        acc[6] += w[u] * vb[u].z;
+        acc[7] += w[u] * vb[u].w;
+      }
+    }
+  }
+  const float inv = wsum == 0.f ? 0.f : 1.f / wsum;
   uint4 o;
   o.x = pack_elem2<kF16>(acc[0] * inv * gs[0], acc[1] * inv * gs[1]);
   o.y = pack_elem2<kF16>(acc[2] * inv * gs[2], acc[3] * inv * gs[3]);
@@ -105,20 +121,38 @@ lse_merge_kernel(const float* __restrict__ O_parts, const float* __restrict__ ls
     lse_out[n] = wsum == 0.f ? -INFINITY : Msub + __logf(wsum);
 }
 
+template <bool kF16>
+cudaError_t launch_merge_t(const MergeArgs& a, long long grid, cudaStream_t stream) {
+  if (!a.after_split) {
+    lse_merge_kernel<kF16><<<dim3(unsigned(grid)), dim3(kWarps * 32), 0, stream>>>(
+        a.O_parts, a.lse_parts, a.S, a.N, static_cast<const uint16_t*>(a.G),
+        static_cast<uint16_t*>(a.out), a.lse_out, 0);
+    return cudaGetLastError();
+  }
+  // Right after the library's split kernel: programmatic dependent launch, so the
+  // merge may be scheduled while that kernel drains; it waits for it in
+  // grid_dependency_wait before reading the parts.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<kF16>, a.O_parts, a.lse_parts, a.S, a.N,
+                            static_cast<const uint16_t*>(a.G), static_cast<uint16_t*>(a.out),
+                            a.lse_out, 1);
+}
+
 }  // namespace
 
 cudaError_t launch_lse_merge(const MergeArgs& a, const LaunchCtl& ctl, cudaStream_t stream) {
   (void)ctl;
   const long long grid = (a.N + kWarps - 1) / kWarps;
-  const auto* G = static_cast<const uint16_t*>(a.G);
-  auto* out = static_cast<uint16_t*>(a.out);
-  if (a.f16)
-    lse_merge_kernel<true><<<dim3(unsigned(grid)), dim3(kWarps * 32), 0, stream>>>(
-        a.O_parts, a.lse_parts, a.S, a.N, G, out, a.lse_out);
-  else
-    lse_merge_kernel<false><<<dim3(unsigned(grid)), dim3(kWarps * 32), 0, stream>>>(
-        a.O_parts, a.lse_parts, a.S, a.N, G, out, a.lse_out);
-  return cudaGetLastError();
+  return a.f16 ? launch_merge_t<true>(a, grid, stream) : launch_merge_t<false>(a, grid, stream);
 }
 
 }  // namespace gqa

@@ -231,6 +231,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = p.ctl.timeout_ns;
+  // Split mode: the merge launched after this kernel (programmatic dependent launch)
+  // may be scheduled once every CTA has started; it still waits for this grid to end.
+  if constexpr (kSplit) asm volatile("griddepcontrol.launch_dependents;");
 
   int b, g, r0, rows_here, n_tiles, j0 = 0, bg;
   // split mode only

@@ -224,3 +224,27 @@ def test_device_range_error_is_recorded():
     assert G.last_device_status() == 0
     out = G.decode(q, kc, vc, g, kv, None, max_rows=1, max_kv_len=20)
     assert_parity(out, ref(x)[0], "after range error")
+
+
+@pytest.mark.parametrize("Hq,Hkv,rows,kv", [(24, 4, [1, 1, 1, 1], [5000, 70, 12000, 900]),
+                                         (16, 2, [8, 32, 1], [3000, 9000, 129])])
+def test_one_call_decode_any_workspace_contents(Hq, Hkv, rows, kv):
+    """The one-call decode launches its merge as a programmatic dependent of the split
+    kernel (the merge waits for the split grid before reading the parts): on both
+    split kernels, with a workspace full of 0xFF bytes, and called repeatedly, it
+    equals split + separately launched merge bit for bit."""
+    x = S.make_decode(len(rows), Hq, Hkv, rows, kv, seed=sum(kv) + 7)
+    q, kc, vc, g, kvd, cu = dev(x)
+    B, T = len(rows), q.shape[0]
+    need = G.decode_workspace_size(B, T, Hq, Hkv, max(rows), max(kv))
+    ws = torch.full((need,), 255, dtype=torch.uint8, device=DEV)
+    op, lp = G.decode_split(q, kc, vc, kvd, cu, max_rows=max(rows), max_kv_len=max(kv))
+    ref = G.lse_merge(op, lp, g).view_as(q)
+    for _ in range(3):
+        out = G.decode(q, kc, vc, g, kvd, cu, max_rows=max(rows), max_kv_len=max(kv),
+                       workspace=ws)
+        assert torch.equal(out, ref)
+    assert G.last_device_status() == 0
+    assert_parity(out, oracle.decode(to_f64(x.q), to_f64(x.k_cache), to_f64(x.v_cache),
+                                     to_f64(x.g), x.kv_lens.tolist(), x.cu_rows.tolist())[0],
+                  "one-call decode")
