@@ -271,6 +271,7 @@ def oracle_decode_sample(x, budget_s=10.0, min_seqs=1):
 
 
 # ----------------------------------------------------------------------------- our arm
+BAL_PARTS = 16     # part slots per row of the one-call decode's balanced shares
 def setup_decode(x, steps, dev, with_rows=False):
     """Device copies and the split plan of a decode (one row per sequence) or, with
     `with_rows`, a verify workload (cu_rows passed to the kernels)."""
@@ -423,16 +424,16 @@ def ours(args):
     # The dominant kernel alone (for the roofline): the same split launch, K more steps,
     # events around gqa_attn_decode_split on the same stream, L2 flushed before each.
     T_, Hq_ = x.q.shape[:2]
-    op = torch.empty((S_, T_ * Hq_, 256), dtype=torch.float32, device=dev)
-    lp = torch.empty((S_, T_ * Hq_), dtype=torch.float32, device=dev)
+    op = torch.empty((BAL_PARTS, T_ * Hq_, 256), dtype=torch.float32, device=dev)
+    lp = torch.empty((BAL_PARTS, T_ * Hq_), dtype=torch.float32, device=dev)
     split_ms = []
     for i in range(args.warmup + args.steps):
         ctx["flush"]()
         a, b = ctx["ev"][i % len(ctx["ev"])]
         a.record()
         G.decode_split(ctx["q"], ctx["kc"], ctx["vc"], ctx["kv"], None, max_rows=1,
-                       max_kv_len=ctx["max_kv"], num_splits=S_, split_keys=C_, o_parts=op,
-                       lse_parts=lp)
+                       max_kv_len=ctx["max_kv"], num_splits=BAL_PARTS, split_keys=0,
+                       o_parts=op, lse_parts=lp)
         b.record()
         b.synchronize()
         if i >= args.warmup:
@@ -632,7 +633,8 @@ def ours(args):
                             "bf16, seed 1",
                 "bytes_per_step": step_bytes,
                 "kv_bytes_per_step": kv_bytes,
-                "split_plan": {"num_splits": S_, "split_keys": C_},
+                "split_plan": {"mode": "balanced shares (one per resident CTA)",
+                               "part_slots": BAL_PARTS},
                 "l2": "flushed before every timed step (256 MiB write, outside the events)",
                 "parallelism": f"replicas x{world} (no data-path collective)",
             },
@@ -647,8 +649,9 @@ def ours(args):
                 "traffic": args.traffic if args.traffic is not None else
                 dram_traffic("decode_split_kernel", int(x.kv_lens.sum()) * x.k_cache.shape[1]),
                 "avg_launch_ms": round(split_avg, 5),
-                "timing": "events around gqa_attn_decode_split alone (same plan and inputs), "
-                          "K steps right after the headline steps, L2 flushed before each",
+                "timing": "events around gqa_attn_decode_split alone in the step's form "
+                          "(balanced shares, 16 part slots), K steps right after the headline "
+                          "steps, L2 flushed before each",
                 "algorithmic_bytes_per_launch": split_bytes,
             },
             "step_note": "one gqa_attn_decode call per step: decode_split_kernel, then "

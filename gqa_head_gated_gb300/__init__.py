@@ -254,7 +254,8 @@ def kv_keep(k_cache, v_cache, kv_lens, cu_rows, keep_idx, cu_keep, kv_lens_out=N
 def decode_split(q, k_cache, v_cache, kv_lens, cu_rows=None, max_rows=None, max_kv_len=None,
                  num_splits=None, split_keys=None, o_parts=None, lse_parts=None):
     """First half of decode: partial results (O/l [S,T*Hq,256] fp32, lse [S,T*Hq]).
-    bf16 or fp16 inputs."""
+    bf16 or fp16 inputs.  split_keys=0 selects balanced shares with num_splits part
+    slots (the one-call decode's form on the mma.sync path)."""
     sfx = _elem(q, "q")
     _need(q, q.dtype, 3, "q")
     _need(k_cache, q.dtype, 4, "k_cache")

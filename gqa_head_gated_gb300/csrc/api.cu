@@ -128,16 +128,31 @@ size_t workspace_bytes_for(int T, int Hq, int S) {
   return size_t(S) * rows * 256 * sizeof(float) + size_t(S) * rows * sizeof(float);
 }
 
+// The one-call decode's choice: the mma.sync kernel (fewer than 64 packed rows per
+// KV group) runs balanced shares when the batch fits the kernel's table.
+bool use_balanced(int B, int Hq, int Hkv, int max_rows) {
+  return !tc_path(Hq, Hkv, max_rows) && B <= kBalancedMaxSeqs;
+}
+
+// Parts per row the one-call decode writes (its workspace holds this many).
+int call_parts(int B, int Hq, int Hkv, int max_rows, int S) {
+  return use_balanced(B, Hq, Hkv, max_rows) ? kBalancedParts : S;
+}
+
 int run_split(const void* Q, const void* Kc, const void* Vc, const int* kv_lens,
               const int* cu_rows, float* O_parts, float* lse_parts, int B, int T, int Hq, int Hkv,
               int Lcap, int max_rows, int max_kv_len, int S, int C, cudaStream_t stream,
-              const unsigned long long* tree_mask, bool f16) {
+              const unsigned long long* tree_mask, bool f16, bool balanced = false) {
   LaunchCtl ctl;
   if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
   DecodeSplitArgs a{Q, Kc, Vc, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
                     max_rows, max_kv_len, S, C};
   a.tree_mask = tree_mask;
   a.f16 = f16;
+  if (balanced) {
+    a.balanced = true;
+    return launch_decode_split(a, ctl, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  }
   if (tc_path(Hq, Hkv, max_rows) && C % tc_split_keys_multiple() == 0) {
     bool encode_failed = false;
     const cudaError_t e = launch_decode_split_tc(a, ctl, stream, &encode_failed);
@@ -196,9 +211,14 @@ int gqa_attn_decode_split_impl(bool f16, const void* Q, const void* Kcache, cons
                                gqa_stream_t stream) {
   const int st = check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
   if (st != GQA_OK) return st;
-  if (num_splits < 1 || split_keys < 64 || split_keys % 64 != 0 ||
-      (long long)num_splits * split_keys < max_kv_len)
+  const bool bal = split_keys == 0;   // balanced shares, num_splits part slots per row
+  if (bal) {
+    if (num_splits < 3) return GQA_ERR_INVALID_ARG;
+    if (!use_balanced(B, Hq, Hkv, max_rows)) return GQA_ERR_UNSUPPORTED;
+  } else if (num_splits < 1 || split_keys < 64 || split_keys % 64 != 0 ||
+             (long long)num_splits * split_keys < max_kv_len) {
     return GQA_ERR_INVALID_ARG;
+  }
   if (T == 0) return GQA_OK;
   if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
       O_parts == nullptr || lse_parts == nullptr)
@@ -213,7 +233,7 @@ int gqa_attn_decode_split_impl(bool f16, const void* Q, const void* Kcache, cons
   if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
   return run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
                    max_rows, max_kv_len, num_splits, split_keys,
-                   static_cast<cudaStream_t>(stream), nullptr, f16);
+                   static_cast<cudaStream_t>(stream), nullptr, f16, bal);
 }
 
 int attn_lse_merge_impl(bool f16, const float* O_parts, const float* lse_parts, int S, int N,
@@ -251,14 +271,16 @@ int gqa_attn_decode_impl(bool f16, const void* Q, const void* Kcache, const void
     return GQA_ERR_INVALID_ARG;
   int S = 0, C = 0;
   plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
+  const bool bal = use_balanced(B, Hq, Hkv, max_rows);
+  if (bal) S = kBalancedParts;
   const size_t need = workspace_bytes_for(T, Hq, S);
   if (workspace == nullptr || workspace_bytes < need) return GQA_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return GQA_ERR_INVALID_ARG;
   float* O_parts = static_cast<float*>(workspace);
   float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
-  int r = gqa_attn_decode_split_impl(f16, Q, Kcache, Vcache, kv_lens, cu_rows, O_parts,
-                                     lse_parts, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, S, C,
-                                     stream);
+  const int r = gqa_attn_decode_split_impl(f16, Q, Kcache, Vcache, kv_lens, cu_rows, O_parts,
+                                           lse_parts, B, T, Hq, Hkv, Lcap, max_rows, max_kv_len,
+                                           S, bal ? 0 : C, stream);
   if (r != GQA_OK) return r;
   return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream,
                              true);
@@ -283,13 +305,16 @@ int gqa_attn_verify_tree_impl(bool f16, const void* Q, const void* Kcache, const
     return GQA_ERR_INVALID_ARG;
   int S = 0, C = 0;
   plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), &S, &C);
+  const bool bal = use_balanced(B, Hq, Hkv, max_rows);
+  if (bal) S = kBalancedParts;
   const size_t need = workspace_bytes_for(T, Hq, S);
   if (workspace == nullptr || workspace_bytes < need) return GQA_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return GQA_ERR_INVALID_ARG;
   float* O_parts = static_cast<float*>(workspace);
   float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
   int r = run_split(Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv, Lcap,
-                    max_rows, max_kv_len, S, C, static_cast<cudaStream_t>(stream), tree_mask, f16);
+                    max_rows, max_kv_len, S, C, static_cast<cudaStream_t>(stream), tree_mask, f16,
+                    bal);
   if (r != GQA_OK) return r;
   return attn_lse_merge_impl(f16, O_parts, lse_parts, S, T * Hq, G, out, lse_out, stream,
                              true);
@@ -436,7 +461,7 @@ size_t gqa_attn_decode_workspace_size(int B, int T, int Hq, int Hkv, int max_row
                                       int max_kv_len) {
   int S = 0, C = 0;
   if (gqa_attn_decode_plan(B, T, Hq, Hkv, max_rows, max_kv_len, &S, &C) != GQA_OK) return 0;
-  return workspace_bytes_for(T, Hq, S);
+  return workspace_bytes_for(T, Hq, call_parts(B, Hq, Hkv, max_rows, S));
 }
 
 int gqa_attn_decode_split(const void* Q, const void* Kcache, const void* Vcache,

@@ -40,8 +40,13 @@ struct Params {
   float* O_parts;
   float* lse_parts;
   int B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, gqa, split_keys, num_splits, n_rb;
+  // Balanced mode (balanced != 0): num_splits is the part capacity per row and
+  // lmax_tiles = ceil(max_kv_len / kTK); see decode_split_kernel.
+  int balanced, lmax_tiles;
   LaunchCtl ctl;
 };
+
+constexpr int kMaxBalancedSeqs = kBalancedMaxSeqs;   // sequences a balanced launch schedules
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -129,14 +134,11 @@ decode_split_kernel(const Params p) {
   // scheduled once every CTA has started; it still waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;");
 
-  int bid = blockIdx.x;
-  const int rb = bid % p.n_rb;
-  bid /= p.n_rb;
-  const int s = bid % p.num_splits;
-  bid /= p.num_splits;
-  const int g = bid % p.Hkv;
-  const int b = bid / p.Hkv;
-
+  // One unit: the packed rows [rb*MB, rb*MB + MB) of (sequence b, KV group g) against
+  // keys [k_lo, min(k_cap, kv_len)), written as part s.  CTA-uniform; returns early
+  // (uniformly) when there is nothing to do.
+  auto run_unit = [&](const int b, const int g, const int rb, const int s, const int k_lo,
+                      const int k_cap) {
   const int kv_len = p.kv_lens[b];
   const int t0 = p.cu_rows ? p.cu_rows[b] : b;
   const int t1 = p.cu_rows ? p.cu_rows[b + 1] : b + 1;
@@ -149,8 +151,11 @@ decode_split_kernel(const Params p) {
   const int P = rows * p.gqa;                 // packed rows of this (b, g)
   const int p0 = rb * MB;
   if (p0 >= P) return;                        // row block past this sequence's rows
-  const int k_lo = s * p.split_keys;
-  const int k_hi = min(k_lo + p.split_keys, kv_len);
+  if (s >= p.num_splits) {                    // cannot happen with a valid plan
+    if (tid == 0) record_status(p.ctl.status, GQA_ERR_DEVICE_RANGE);
+    return;
+  }
+  const int k_hi = min(k_cap, kv_len);
 
   // Visible keys of each packed row of the block (0 for padding rows).
   // Chain: row i sees keys < kv_len - rows + i + 1.  Tree: keys before the new rows,
@@ -397,6 +402,95 @@ decode_split_kernel(const Params p) {
     *reinterpret_cast<float4*>(p.O_parts + part * 256 + c4) = acc;
     if (c4 == 0) p.lse_parts[part] = (Msub + __log2f(L)) * kLn2;
   }
+  };   // run_unit
+
+  if (!p.balanced) {
+    // One unit per CTA: (b, g, split s, row block rb) from the block index.
+    int bid = blockIdx.x;
+    const int rb = bid % p.n_rb;
+    bid /= p.n_rb;
+    const int s = bid % p.num_splits;
+    bid /= p.num_splits;
+    const int g = bid % p.Hkv;
+    const int b = bid / p.Hkv;
+    run_unit(b, g, rb, s, s * p.split_keys, s * p.split_keys + p.split_keys);
+    return;
+  }
+
+  // Balanced mode: the key ranges of all (sequence, KV group, row block) segments,
+  // in tiles of kTK keys, are laid end to end (sequence-major) and cut into equal
+  // contiguous shares, one per CTA, so every CTA streams the same number of tiles
+  // whatever the sequence lengths.  A share that crosses segments yields one part per
+  // piece; a piece's part index is its CTA's position among the CTAs sharing the
+  // segment, and the CTA that ends a segment marks the unused part slots empty.
+  __shared__ int s_base[kMaxBalancedSeqs + 1];
+  for (int b = tid; b < p.B; b += kThreads) {
+    const int kv = p.kv_lens[b];
+    const int t0 = p.cu_rows ? p.cu_rows[b] : b;
+    const int rows = (p.cu_rows ? p.cu_rows[b + 1] : b + 1) - t0;
+    const bool ok = rows >= 0 && rows <= p.max_rows && kv >= rows && kv <= p.max_kv_len &&
+                    kv <= p.Lcap && t0 >= 0 && t0 + rows <= p.T;
+    const int nrb = (rows * p.gqa + MB - 1) / MB;
+    s_base[b + 1] = ok ? p.Hkv * nrb * ((kv + kTK - 1) / kTK) : 0;
+    if (!ok && rows != 0) record_status(p.ctl.status, GQA_ERR_DEVICE_RANGE);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    s_base[0] = 0;
+    for (int b = 0; b < p.B; ++b) s_base[b + 1] += s_base[b];
+  }
+  __syncthreads();
+  const long long W = s_base[p.B];
+  // Shares of at least lmax_tiles / (num_splits - 2) tiles keep every segment within
+  // num_splits parts; every share holds at least one tile.
+  long long n_cta = (W * (p.num_splits - 2)) / max(1, p.lmax_tiles);
+  n_cta = min(min(n_cta, W), (long long)gridDim.x);
+  n_cta = max(n_cta, 1LL);
+  const long long i = blockIdx.x;
+  if (i >= n_cta || W == 0) return;
+  long long pos = W * i / n_cta;
+  const long long r1 = W * (i + 1) / n_cta;
+  while (pos < r1) {
+    int b = 0;
+    {
+      int lo = 0, hi = p.B - 1;        // last b with s_base[b] <= pos
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_base[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      b = lo;
+    }
+    const int kv = p.kv_lens[b];
+    const int t0 = p.cu_rows ? p.cu_rows[b] : b;
+    const int rows = (p.cu_rows ? p.cu_rows[b + 1] : b + 1) - t0;
+    const int nrb = (rows * p.gqa + MB - 1) / MB;
+    const long long seg_len = (kv + kTK - 1) / kTK;
+    const long long off = pos - s_base[b];
+    const long long seg = off / seg_len;
+    const int g = int(seg / nrb);
+    const int rb = int(seg % nrb);
+    const long long seg_start = s_base[b] + seg * seg_len;
+    const long long seg_end = seg_start + seg_len;
+    const long long piece_end = min(r1, seg_end);
+    const long long i0 = ((seg_start + 1) * n_cta + W - 1) / W - 1;   // CTA holding its first tile
+    const int s = int(i - i0);
+    run_unit(b, g, rb, s, int(pos - seg_start) * kTK, int(piece_end - seg_start) * kTK);
+    if (piece_end == seg_end) {
+      // Part slots s+1 .. num_splits-1 of this segment's rows are empty.
+      const int P = rows * p.gqa;
+      const int p0 = rb * MB;
+      const int nr = min(MB, P - p0);
+      const int nfill = p.num_splits - 1 - s;
+      for (int idx = tid; idx < nfill * nr; idx += kThreads) {
+        const int sp = s + 1 + idx / nr;
+        const int pp = p0 + idx % nr;
+        const size_t n = size_t(t0 + pp / p.gqa) * p.Hq + g * p.gqa + pp % p.gqa;
+        p.lse_parts[size_t(sp) * size_t(p.T) * p.Hq + n] = -INFINITY;
+      }
+    }
+    __syncthreads();                   // shared buffers are reused by the next piece
+    pos = piece_end;
+  }
 }
 
 template <int WR, int WK, bool kF16>
@@ -406,6 +500,18 @@ cudaError_t launch_t(const Params& p, cudaStream_t stream, long long grid) {
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<WR, WK, kF16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
+  if (p.balanced) {
+    // One CTA per resident slot: the shares are cut on the device.
+    int per_sm = 0, dev = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<WR, WK, kF16>,
+                                                      kThreads, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    grid = (long long)(per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+  }
   decode_split_kernel<WR, WK, kF16><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(p);
   return cudaGetLastError();
 }
@@ -440,6 +546,8 @@ cudaError_t launch_decode_split(const DecodeSplitArgs& a, const LaunchCtl& ctl,
   p.split_keys = a.split_keys;
   p.num_splits = a.num_splits;
   p.ctl = ctl;
+  p.balanced = a.balanced ? 1 : 0;
+  p.lmax_tiles = (a.max_kv_len + kTK - 1) / kTK;
   const int MB = decode_rows_per_cta(a.max_rows * p.gqa);
   p.n_rb = (a.max_rows * p.gqa + MB - 1) / MB;
   const long long grid = (long long)a.B * a.Hkv * a.num_splits * p.n_rb;

@@ -50,7 +50,14 @@ struct DecodeSplitArgs {
   // k visible); null for chain verify / decode.
   const unsigned long long* tree_mask = nullptr;
   bool f16 = false;   // fp16 instead of bf16 elements
+  // mma.sync kernel only: equal shares of all sequences' key tiles per CTA instead
+  // of one (b, g, split, row block) unit per CTA; num_splits is then the part
+  // capacity per row (>= 3) and split_keys is unused.  B <= kBalancedMaxSeqs.
+  bool balanced = false;
 };
+
+constexpr int kBalancedMaxSeqs = 256;
+constexpr int kBalancedParts = 16;
 
 // Packed query rows (heads x rows of one KV group) per decode CTA: 16, 32 or 64.
 int decode_rows_per_cta(int packed_rows);
