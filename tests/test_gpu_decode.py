@@ -271,3 +271,28 @@ def test_balanced_shares_extreme_lengths(lens):
     r_out, r_lse = ref(x)
     assert_parity(out, r_out, f"balanced {B} seqs")
     np.testing.assert_allclose(to_f64(lse), r_lse, rtol=0, atol=2e-3)
+
+
+@pytest.mark.parametrize("rows,lens", [
+    ([8, 1, 32, 3], [24000, 9, 200, 3000]),          # one range dwarfs the rest
+    ([16] * 40, [130 + 977 * i for i in range(40)]),  # a ladder over 40 sequences
+    ([64, 2], [70, 64000]),                           # 64 rows over a short cache
+])
+def test_tcgen05_path_extreme_lengths(rows, lens):
+    """Verify rows on the tcgen05 split kernel (>= 64 packed rows per group) with
+    extreme length mixes, chain and tree masks, against the oracle."""
+    B = len(rows)
+    x = S.make_decode(B, 16, 2, rows, lens, Lcap=max(lens) + 5, seed=sum(lens) % 1000)
+    out, lse = run(x, lse=True)
+    r_out, r_lse = ref(x)
+    assert_parity(out, r_out, f"tcgen05 path {rows}")
+    np.testing.assert_allclose(to_f64(lse), r_lse, rtol=0, atol=2e-3)
+    masks = S.random_tree_masks(rows, 3)
+    q, kc, vc, g, kvd, cu = dev(x)
+    tm = torch.tensor([m - (1 << 64) if m >= 1 << 63 else m for m in masks], dtype=torch.int64,
+                      device=DEV)
+    t_out = G.verify_tree(q, kc, vc, g, kvd, cu, tm, max_rows=max(rows), max_kv_len=max(lens))
+    assert G.last_device_status() == 0
+    t_ref = oracle.decode_tree(to_f64(x.q), to_f64(x.k_cache), to_f64(x.v_cache), to_f64(x.g),
+                               x.kv_lens.tolist(), x.cu_rows.tolist(), masks)[0]
+    assert_parity(t_out, t_ref, f"tcgen05 path tree {rows}")
