@@ -649,6 +649,10 @@ def ours(args):
                 "traffic": args.traffic if args.traffic is not None else
                 dram_traffic("decode_split_kernel", int(x.kv_lens.sum()) * x.k_cache.shape[1]),
                 "avg_launch_ms": round(split_avg, 5),
+                "launch": {"grid": 2 * torch.cuda.get_device_properties(dev).multi_processor_count,
+                           "block": 128, "dynamic_smem_bytes": 16 * 512 + 3 * 2 * 32 * 512,
+                           "packed_rows_per_cta": 16, "tile_keys": 32, "stages": 3,
+                           "part_slots": BAL_PARTS},
                 "timing": "events around gqa_attn_decode_split alone in the step's form "
                           "(balanced shares, 16 part slots), K steps right after the headline "
                           "steps, L2 flushed before each",
@@ -672,6 +676,9 @@ def ours(args):
                 "flops_per_call": flops,
                 "avg_ms": round(pf_avg, 4),
                 "steps": pf_steps,
+                "launch": {"grid": -(-8192 // (128 // 6)) * 4, "block": 320,
+                           "rows_per_tile": 128 // 6, "heads_per_tile": 6, "tile_keys": 128,
+                           "tmem_columns": 512},
                 "roofline": {"kernel": "attn_tc_kernel<prefill>", "bound": "tensor",
                              "achieved": round(pf_tflops, 2), "peak": bf16_peak,
                              "peak_source": f"{peak_src} bf16_tflops (burst)",
