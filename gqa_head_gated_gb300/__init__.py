@@ -174,8 +174,8 @@ def decode(q, k_cache, v_cache, g, kv_lens, cu_rows=None, max_rows=None, max_kv_
         _need(g, q.dtype, 3, "g")
     T, Hq, B, Hkv, Lcap, max_rows, max_kv_len = _decode_sizes(q, k_cache, kv_lens, cu_rows,
                                                                max_rows, max_kv_len)
-    need = decode_workspace_size(B, T, Hq, Hkv, max_rows, max_kv_len)
-    if workspace is None:
+    if workspace is None:    # (a given workspace is checked by the library itself)
+        need = decode_workspace_size(B, T, Hq, Hkv, max_rows, max_kv_len)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if out is None:
         out = torch.empty_like(q)

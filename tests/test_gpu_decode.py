@@ -275,7 +275,7 @@ def test_balanced_shares_extreme_lengths(lens):
 
 @pytest.mark.parametrize("rows,lens", [
     ([8, 1, 32, 3], [24000, 9, 200, 3000]),          # one range dwarfs the rest
-    ([16] * 40, [130 + 977 * i for i in range(40)]),  # a ladder over 40 sequences
+    ([16] * 12, [130 + 2777 * i for i in range(12)]), # a ladder over 12 sequences
     ([64, 2], [70, 64000]),                           # 64 rows over a short cache
 ])
 def test_tcgen05_path_extreme_lengths(rows, lens):
