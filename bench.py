@@ -360,6 +360,63 @@ def bench_e2e_decode(x, steps, warmup, dev):
     return sum(times), h2d, d2h, ok
 
 
+def bench_decode_graphs(x, steps, warmup, dev):
+    """The headline decode step and its end-to-end form captured once in CUDA graphs
+    (after eager warm-up calls) and replayed: the step's device time without host
+    launch overhead between its operations."""
+    import gqa_head_gated_gb300 as G
+    kc, vc = x.k_cache.to(dev), x.v_cache.to(dev)
+    nq, ng, nkv = x.q.numel() * 2, x.g.numel() * 2, x.kv_lens.numel() * 4
+    hin = torch.empty(nq + ng + nkv, dtype=torch.uint8).pin_memory()
+    hin[:nq].copy_(x.q.reshape(-1).view(torch.uint8))
+    hin[nq:nq + ng].copy_(x.g.reshape(-1).view(torch.uint8))
+    hin[nq + ng:].copy_(x.kv_lens.view(torch.uint8))
+    din = torch.empty_like(hin, device=dev)
+    din.copy_(hin)
+    dq = din[:nq].view(torch.bfloat16).view(x.q.shape)
+    dg = din[nq:nq + ng].view(torch.bfloat16).view(x.g.shape)
+    dkv = din[nq + ng:].view(torch.int32)
+    hout = torch.empty_like(x.q).pin_memory()
+    max_kv = int(x.kv_lens.max())
+    B, Hkv = kc.shape[0], kc.shape[1]
+    T, Hq = x.q.shape[0], x.q.shape[1]
+    ws = torch.empty(G.decode_workspace_size(B, T, Hq, Hkv, 1, max_kv), dtype=torch.uint8,
+                     device=dev)
+    dout = torch.empty_like(dq)
+    flush = L2Flush(dev)
+
+    def kernel_step():
+        G.decode(dq, kc, vc, dg, dkv, None, max_rows=1, max_kv_len=max_kv, workspace=ws, out=dout)
+
+    def e2e_step():
+        din.copy_(hin, non_blocking=True)
+        kernel_step()
+        hout.copy_(dout, non_blocking=True)
+
+    res = {}
+    for name, fn in (("step", kernel_step), ("e2e", e2e_step)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        times = []
+        for i in range(warmup + steps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            b.synchronize()
+            if i >= warmup:
+                times.append(a.elapsed_time(b))
+        res[name] = sum(times) / len(times)
+        del graph
+    res["finite"] = bool(torch.isfinite(hout.float()).all().item())
+    return res
+
+
 def bench_prefill(x, steps, warmup, dev, e2e=True):
     import gqa_head_gated_gb300 as G
     q, k, v, g = (t.to(dev) for t in (x.q, x.k, x.v, x.g))
@@ -457,6 +514,13 @@ def ours(args):
     e2e_ms = max_over_ranks(world, e2e_ms)
     e2e_val = world * step_bytes * args.steps / (e2e_ms / 1e3) / 1e9
 
+    graphs = None
+    if not args.no_extra:
+        try:
+            graphs = bench_decode_graphs(x, args.steps, args.warmup, dev)
+        except Exception as exc:   # noqa: BLE001 - reported, not fatal
+            graphs = {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
     # prefill side of the metric (27B-shape prefill)
     pf = S.prefill_27b()
     flops = prefill_flops(pf)
@@ -470,6 +534,18 @@ def ours(args):
 
     # the other throughput workloads of the metric, inside the same line
     more = {}
+    if graphs is not None:
+        if "error" in graphs:
+            more["decode_27b_cuda_graph"] = graphs
+        else:
+            more["decode_27b_cuda_graph"] = {
+                "workload": "the headline decode step and its end-to-end form (pinned inputs "
+                            "in, out back) captured once in CUDA graphs and replayed",
+                "value": round(step_bytes / (graphs["step"] / 1e3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(graphs["step"], 5),
+                "e2e_value": round(step_bytes / (graphs["e2e"] / 1e3) / 1e9, 2),
+                "e2e_ms_per_step": round(graphs["e2e"], 5),
+                "outputs_finite": graphs["finite"]}
     if not args.no_extra:
         cp = S.chunked_prefill_35b()
         cp_flops = prefill_flops(cp)
