@@ -271,6 +271,8 @@ def oracle_decode_sample(x, budget_s=10.0, min_seqs=1):
 
 
 # ----------------------------------------------------------------------------- our arm
+DECODE_WORKLOAD = ("27B-shape decode: B=16, Hq=24, Hkv=4, head_dim=256, 1 row/seq, kv_lens "
+                   "uniform [1024,32768] (sum 297,628), cache [16,4,32768,256] bf16, seed 1")
 BAL_PARTS = 16     # part slots per row of the one-call decode's balanced shares
 def setup_decode(x, steps, dev, with_rows=False):
     """Device copies and the split plan of a decode (one row per sequence) or, with
@@ -709,9 +711,7 @@ def ours(args):
             "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 Q/K/V, G ~ N(0,2)); no dataset",
             "config": {
-                "workload": "27B-shape decode: B=16, Hq=24, Hkv=4, head_dim=256, 1 row/seq, "
-                            "kv_lens uniform [1024,32768] (sum 297,628), cache [16,4,32768,256] "
-                            "bf16, seed 1",
+                "workload": DECODE_WORKLOAD,
                 "bytes_per_step": step_bytes,
                 "kv_bytes_per_step": kv_bytes,
                 "split_plan": {"mode": "balanced shares (one per resident CTA)",
@@ -816,8 +816,10 @@ def reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, G ~ N(0,2)); no dataset",
-        "config": {"workload": "27B-shape decode: B=16, Hq=24, Hkv=4, head_dim=256, 1 row/seq, "
-                               "kv_lens uniform [1024,32768], seed 1 (bounded sample per step)"},
+        "config": {"workload": DECODE_WORKLOAD,
+                   "bytes_per_step": decode_bytes(x)[1],
+                   "sample": "each step a bounded sample of whole sequences (see cpu_baseline)",
+                   "parallelism": "rank 0 only (host cores)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": _CORES,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
