@@ -59,10 +59,6 @@ bool make_ctl(LaunchCtl* ctl) {
 
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
-// Decode split plan: aim for about three waves of resident CTAs over the
-// (sequence, group, row block) units (two CTAs fit per SM up to 32 packed rows, one
-// above), so that ragged kv lengths still leave enough CTAs to balance the SMs;
-// splits are whole 64-key steps.
 // Decode / verify groups with at least this many packed rows (new rows x query heads
 // per KV group) run on the tcgen05 kernel; fewer run on the mma.sync split kernel,
 // which is memory-bound there already.
@@ -73,6 +69,11 @@ bool tc_path(int Hq, int Hkv, int max_rows) {
   return (long long)max_rows * (Hq / Hkv) >= kTcMinPackedRows && Hq / Hkv <= 128;
 }
 
+// Fixed-split decode plan (gqa_attn_decode_plan, and the one-call decode when it does
+// not run balanced shares): aim for about three waves of resident CTAs over the
+// (sequence, group, row block) units (two CTAs fit per SM up to 32 packed rows, one
+// above), so that ragged kv lengths still leave enough CTAs to balance the SMs;
+// splits are whole 64-key steps (128-key tiles on the tcgen05 path).
 int plan_decode(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int num_sms, int* S,
                 int* C) {
   const int gqa = Hq / Hkv;

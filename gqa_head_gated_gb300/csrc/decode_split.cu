@@ -16,6 +16,11 @@
 // padding is never read.  Scores and P.V run on bf16 or fp16 mma.sync (m16n8k16,
 // fp32 accumulate); the online softmax is fp32 with quad-shuffle row reductions
 // and rescales at every tile, so P <= 1 in either element type.
+//
+// Work split: either one (b, g, split, row block) unit per CTA (fixed splits of
+// `split_keys`), or balanced shares (the one-call decode): all units' key tiles laid
+// end to end and cut into one equal contiguous share per resident CTA, a share that
+// crosses units yielding one part per piece.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
