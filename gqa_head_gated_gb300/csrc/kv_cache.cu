@@ -1,8 +1,9 @@
 // KV-cache maintenance around decode / verify: append new rows after the keys a
 // sequence holds, and keep the accepted draft rows after verification (TensorFold
 // PR #1009, "Receipt": packing, append and keep are compared bit for bit; control
-// "an append one row late").  Both are plain 16-byte copies, one warp per 512-byte
-// key row; sequence lengths live on the device and are range-checked there.
+// "an append one row late").  Both are plain 16-byte copies of 512-byte key rows by
+// whole warps (append: four rows per warp; keep: one sequence and KV head per warp);
+// sequence lengths live on the device and are range-checked there.
 #include <cuda_runtime.h>
 
 #include "gqa_attn.h"
@@ -23,28 +24,48 @@ __device__ __forceinline__ int seq_of(const int* cu_rows, int B, int t) {
   return lo;
 }
 
-// One warp per (new token, KV head): K and V rows of 512 bytes, 16 bytes per lane.
+constexpr int kRowsPerWarp = 4;   // (token, KV head) rows per warp: 8 loads in flight per lane
+
+// One warp per kRowsPerWarp consecutive (new token, KV head) items: K and V rows of
+// 512 bytes, 16 bytes per lane; all loads are issued before the stores.
 __global__ void __launch_bounds__(kWarps * 32)
 kv_append_kernel(const uint4* __restrict__ Knew, const uint4* __restrict__ Vnew,
                  const int* __restrict__ cu_rows, const int* __restrict__ kv_lens,
                  uint4* __restrict__ Kc, uint4* __restrict__ Vc, int B, int T, int Hkv,
                  int Lcap, LaunchCtl ctl) {
-  const int w = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const long long w0 = ((long long)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
   const int lane = threadIdx.x & 31;
-  if (w >= T * Hkv) return;
-  const int t = w / Hkv;
-  const int g = w - t * Hkv;
-  const int b = cu_rows ? seq_of(cu_rows, B, t) : t;
-  const int i = cu_rows ? t - __ldg(cu_rows + b) : 0;
-  const int pos = __ldg(kv_lens + b) + i;
-  if (pos < 0 || pos >= Lcap) {
-    if (lane == 0) record_status(ctl.status, GQA_ERR_DEVICE_RANGE);
-    return;
+  const long long n_items = (long long)T * Hkv;
+  uint4 kv[kRowsPerWarp][2];
+  size_t dst[kRowsPerWarp];
+  bool live[kRowsPerWarp];
+#pragma unroll
+  for (int u = 0; u < kRowsPerWarp; ++u) {
+    const long long w = w0 + u;
+    live[u] = false;
+    dst[u] = 0;
+    if (w >= n_items) continue;
+    const int t = int(w / Hkv);
+    const int g = int(w - (long long)t * Hkv);
+    const int b = cu_rows ? seq_of(cu_rows, B, t) : t;
+    const int i = cu_rows ? t - __ldg(cu_rows + b) : 0;
+    const int pos = __ldg(kv_lens + b) + i;
+    if (pos < 0 || pos >= Lcap) {
+      if (lane == 0) record_status(ctl.status, GQA_ERR_DEVICE_RANGE);
+      continue;
+    }
+    const size_t src = (size_t(t) * Hkv + g) * 32 + lane;
+    dst[u] = ((size_t(b) * Hkv + g) * size_t(Lcap) + pos) * 32 + lane;
+    kv[u][0] = __ldg(Knew + src);
+    kv[u][1] = __ldg(Vnew + src);
+    live[u] = true;
   }
-  const size_t src = (size_t(t) * Hkv + g) * 32 + lane;
-  const size_t dst = ((size_t(b) * Hkv + g) * size_t(Lcap) + pos) * 32 + lane;
-  Kc[dst] = __ldg(Knew + src);
-  Vc[dst] = __ldg(Vnew + src);
+#pragma unroll
+  for (int u = 0; u < kRowsPerWarp; ++u) {
+    if (!live[u]) continue;
+    Kc[dst[u]] = kv[u][0];
+    Vc[dst[u]] = kv[u][1];
+  }
 }
 
 // One warp per (sequence, KV head): kept draft rows move to the front of the draft
@@ -113,7 +134,8 @@ int gqa_kv_append(const void* Knew, const void* Vnew, const int* cu_rows, const 
     return GQA_ERR_INVALID_ARG;
   LaunchCtl ctl;
   if (!make_launch_ctl(&ctl)) return GQA_ERR_CUDA;
-  const long long grid = ((long long)T * Hkv + kWarps - 1) / kWarps;
+  const long long per_cta = (long long)kWarps * kRowsPerWarp;
+  const long long grid = ((long long)T * Hkv + per_cta - 1) / per_cta;
   kv_append_kernel<<<dim3(unsigned(grid)), kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(Knew), static_cast<const uint4*>(Vnew), cu_rows, kv_lens,
       static_cast<uint4*>(Kcache), static_cast<uint4*>(Vcache), B, T, Hkv, Lcap, ctl);
