@@ -80,6 +80,7 @@ constexpr int kChunkBytes = kN * 128;         // K/V: kN rows x 64 bf16 per colu
 constexpr int kTileBytes = 4 * kChunkBytes;   // kN keys x 256 bf16
 constexpr int kHalf = kN / 2;                 // keys per softmax thread per tile
 static_assert(kN == 64 || kN == 128, "key tile of 64 or 128");
+static_assert(kSlots * kTileBytes >= kQBytes, "the output tile is staged in the K/V ring");
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmO = 0;
@@ -106,6 +107,8 @@ struct __align__(1024) Smem {
   uint64_t o_final;
   uint64_t drain;
   uint64_t v_clean;            // split mode: the last V tile's padding rows are zeroed
+  uint64_t q_free;             // prefill: every S product has read Q (its buffer takes G)
+  uint64_t g_full;             // prefill: the gate tile has landed in Q's buffer
   uint32_t tmem_base;
   int abort;
   int zero;
@@ -224,7 +227,8 @@ __device__ __forceinline__ void apply_mask_row(uint32_t (&s)[kN_], const E* row,
 template <bool kSplit, bool kF16, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const Params p) {
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+               const __grid_constant__ CUtensorMap tmO, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
@@ -301,6 +305,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     ptx::mbar_init(&sm.o_final, 1);
     ptx::mbar_init(&sm.drain, 1);
     ptx::mbar_init(&sm.v_clean, 1);
+    ptx::mbar_init(&sm.q_free, 1);
+    ptx::mbar_init(&sm.g_full, 1);
     sm.abort = 0;
     sm.zero = 0;
     ptx::fence_mbar_init();
@@ -319,10 +325,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     Ring rk{0, 0u, 0, kKS, 0};
     Ring rv{0, 0u, 0, kVS, kKS};
     bool issued_all = false;
+    bool g_issued = false;
     if (lane == 0) {
       ptx::prefetch_tmap(&tmQ);
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
+      if constexpr (!kSplit) {
+        ptx::prefetch_tmap(&tmG);
+        ptx::prefetch_tmap(&tmO);
+      }
       const uint32_t q_bytes = 4u * 128u * uint32_t(p.R * p.gqa);
       ptx::mbar_arrive_expect_tx(&sm.q_full, q_bytes);
       for (int dc = 0; dc < 4; ++dc) {
@@ -351,6 +362,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         r.advance();
       }
       issued_all = rv.count == n_tiles;
+      if constexpr (!kSplit) {
+        // Prefill: the gate tile (same box as Q) goes into Q's buffer once every S
+        // product has read Q; it lands while the last P.V products run.
+        if (p.G != nullptr && issued_all) {
+          if (ptx::mbar_wait(&sm.q_free, 0, tmo, &sm.abort)) {
+            ptx::mbar_arrive_expect_tx(&sm.g_full, q_bytes);
+            for (int dc = 0; dc < 4; ++dc)
+              ptx::tma_load_4d(sm.q + dc * kQChunk, &tmG, &sm.g_full, dc * 64, r0, g * p.gqa, b);
+            g_issued = true;
+          } else {
+            fail(sm, p);
+          }
+        }
+      }
     }
     if constexpr (kSplit) {
       // Split mode: a tile holding cache rows at or past kv_len can only be the CTA's
@@ -390,6 +415,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         for (int c = max(0, r->count - r->n); c < r->count; ++c)
           ptx::mbar_wait(&sm.kv_full[r->base + c % r->n], uint32_t(c / r->n) & 1u, tmo, &sm.zero);
       ptx::mbar_wait(&sm.q_full, 0, tmo, &sm.zero);
+      if (g_issued) ptx::mbar_wait(&sm.g_full, 0, tmo, &sm.zero);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -448,6 +474,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int j = 1; ok && j < n_tiles; ++j) {
         ok = issue_s(j);
         if (ok) ok = issue_pv(j - 1);
+      }
+      if constexpr (!kSplit) {
+        if (ok) ptx::tc_commit(&sm.q_free);   // every S product issued: Q may be overwritten
       }
       if (ok) ok = issue_pv(n_tiles - 1);
       if (ok) {
@@ -621,54 +650,52 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     sm.ok[pb][half][row] = fin ? 1 : 0;
     ptx::named_bar_sync(bar_id, 64);
     fin = fin && sm.ok[pb][half ^ 1][row];
+    // Prefill: the gate tile arrives by TMA in Q's buffer (same swizzled layout as Q),
+    // and the output tile is staged in the K/V ring (free once O is final) for one
+    // TMA store: row m's 16-byte chunk c of column block dc sits at dc * kQChunk +
+    // m * 128 + (c ^ (m & 7)) * 16 in both.
+    uint8_t* const stage = &sm.kv[0][0];
+    if constexpr (!kSplit) {
+      if (p.G != nullptr) fin = warp_all(ptx::mbar_wait(&sm.g_full, 0, tmo, &sm.abort)) && fin;
+    }
     if (fin) {
       ptx::tc_fence_after();
       const float l_tot = l_part + sm.red[pb][half ^ 1][row];
       // l_tot is 0 exactly when the row saw no key, NaN when it saw a NaN score.
       const float inv_l = l_tot == 0.f ? 0.f : 1.f / l_tot;
       if constexpr (!kSplit) {
-        const int h = g * p.gqa + hh;
-        const size_t row_off = (size_t(b) * p.Hq + h) * size_t(p.Lq) + size_t(q);
-#pragma unroll 1
+        const size_t row_off =
+            (size_t(b) * p.Hq + size_t(g * p.gqa + hh)) * size_t(p.Lq) + size_t(q);
+#pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
           ptx::tmem_ld32_wait(trow + kTmO + 128u * half + 32u * cc, o);
-          if (valid) {
-            const int col0 = half * 128 + cc * 32;
-            float gs[32];
+          const int dc = half * 2 + (cc >> 1);   // columns half*128 + cc*32 .. +31
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int c = (cc & 1) * 4 + v;
+            const uint32_t off =
+                uint32_t(dc) * kQChunk + uint32_t(row) * 128u + (uint32_t(c ^ (row & 7)) << 4);
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
             if (p.G != nullptr) {
-              const uint4* gp = reinterpret_cast<const uint4*>(p.G + row_off * kHeadDim + col0);
+              const uint4 u = *reinterpret_cast<const uint4*>(sm.q + off);
+              w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+            }
+            uint32_t r[4];
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const uint4 u = __ldg(gp + v);
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 f = unpack_elem2<kF16>(w[e]);
-                  gs[v * 8 + 2 * e] = gate_sigmoid(f.x);
-                  gs[v * 8 + 2 * e + 1] = gate_sigmoid(f.y);
-                }
+            for (int e = 0; e < 4; ++e) {
+              float2 gs = make_float2(1.f, 1.f);
+              if (p.G != nullptr) {
+                const float2 f = unpack_elem2<kF16>(w[e]);
+                gs = make_float2(gate_sigmoid(f.x), gate_sigmoid(f.y));
               }
-            } else {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) gs[c] = 1.f;
+              r[e] = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 2 * e]) * inv_l * gs.x,
+                                      __uint_as_float(o[v * 8 + 2 * e + 1]) * inv_l * gs.y);
             }
-            uint4* op = reinterpret_cast<uint4*>(p.out + row_off * kHeadDim + col0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 u;
-              u.x = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 0]) * inv_l * gs[v * 8 + 0],
-                                __uint_as_float(o[v * 8 + 1]) * inv_l * gs[v * 8 + 1]);
-              u.y = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 2]) * inv_l * gs[v * 8 + 2],
-                                __uint_as_float(o[v * 8 + 3]) * inv_l * gs[v * 8 + 3]);
-              u.z = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 4]) * inv_l * gs[v * 8 + 4],
-                                __uint_as_float(o[v * 8 + 5]) * inv_l * gs[v * 8 + 5]);
-              u.w = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 6]) * inv_l * gs[v * 8 + 6],
-                                __uint_as_float(o[v * 8 + 7]) * inv_l * gs[v * 8 + 7]);
-              op[v] = u;
-            }
+            *reinterpret_cast<uint4*>(stage + off) = make_uint4(r[0], r[1], r[2], r[3]);
           }
         }
+        ptx::fence_proxy_async_smem();   // the staged tile is read by the TMA store
         if (valid && half == 0 && p.lse != nullptr)
           p.lse[row_off] = l_tot == 0.f ? -INFINITY : (m_run + __log2f(l_tot)) * kLn2;
       } else {
@@ -695,6 +722,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
     } else {
       fail(sm, p);
+    }
+    if constexpr (!kSplit) {
+      // Every softmax thread has staged its rows: one thread stores the tile (rows
+      // past Lq fall outside the tensor and are not written) and waits until the
+      // copy has read shared memory, which stays allocated until then.
+      ptx::named_bar_sync(5, 256);
+      if (threadIdx.x == 64 && *reinterpret_cast<volatile int*>(&sm.abort) == 0) {
+        for (int dc = 0; dc < 4; ++dc)
+          ptx::tma_store_4d(&tmO, stage + dc * kQChunk, dc * 64, r0, g * p.gqa, b);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_group_read0();
+      }
     }
   }
 
@@ -739,13 +778,14 @@ bool encode_16b(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank,
 
 template <bool kSplit, bool kF16, bool kMask = false>
 cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const Params& p, long long grid, cudaStream_t stream) {
+                      const CUtensorMap& tg, const CUtensorMap& to, const Params& p,
+                      long long grid, cudaStream_t stream) {
   const size_t smem = sizeof(Smem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kSplit, kF16, kMask>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   attn_tc_kernel<kSplit, kF16, kMask>
-      <<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, p);
+      <<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, tg, to, p);
   return cudaGetLastError();
 }
 
@@ -761,12 +801,16 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
   }
   const int gqa = a.Hq / a.Hkv;
   const int R = prefill_rows_per_tile(gqa);
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tg, to;
   {
+    // Q, G and out [B, Hq, Lq, 256]: a box is R rows x the group's GQA heads x 64 dims.
     const cuuint64_t dims[4] = {256, cuuint64_t(a.Lq), cuuint64_t(a.Hq), cuuint64_t(a.B)};
     const cuuint64_t str[3] = {512, cuuint64_t(a.Lq) * 512, cuuint64_t(a.Hq) * a.Lq * 512};
     const cuuint32_t box[4] = {64, cuuint32_t(R), cuuint32_t(gqa), 1};
     if (!encode_16b(fn, &tq, a.Q, 4, dims, str, box, a.f16)) *encode_failed = true;
+    if (!encode_16b(fn, &tg, a.G != nullptr ? a.G : a.Q, 4, dims, str, box, a.f16))
+      *encode_failed = true;
+    if (!encode_16b(fn, &to, a.out, 4, dims, str, box, a.f16)) *encode_failed = true;
   }
   {
     // Only keys a row of the call can see are addressable; TMA zero-fills the rest.
@@ -805,10 +849,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
 
   const long long grid = (long long)p.n_rtiles * a.B * a.Hkv;
   if (a.masked)
-    return a.f16 ? launch_tc<false, true, true>(tq, tk, tv, p, grid, stream)
-                 : launch_tc<false, false, true>(tq, tk, tv, p, grid, stream);
-  return a.f16 ? launch_tc<false, true>(tq, tk, tv, p, grid, stream)
-               : launch_tc<false, false>(tq, tk, tv, p, grid, stream);
+    return a.f16 ? launch_tc<false, true, true>(tq, tk, tv, tg, to, p, grid, stream)
+                 : launch_tc<false, false, true>(tq, tk, tv, tg, to, p, grid, stream);
+  return a.f16 ? launch_tc<false, true>(tq, tk, tv, tg, to, p, grid, stream)
+               : launch_tc<false, false>(tq, tk, tv, tg, to, p, grid, stream);
 }
 
 int tc_split_keys_multiple() { return kN; }
@@ -861,8 +905,9 @@ cudaError_t launch_decode_split_tc(const DecodeSplitArgs& a, const LaunchCtl& ct
   p.ctl = ctl;
 
   const long long grid = (long long)a.B * a.Hkv * a.num_splits * p.n_rtiles;
-  return a.f16 ? launch_tc<true, true>(tq, tk, tv, p, grid, stream)
-               : launch_tc<true, false>(tq, tk, tv, p, grid, stream);
+  // The gate and output maps are not used in split mode.
+  return a.f16 ? launch_tc<true, true>(tq, tk, tv, tq, tq, p, grid, stream)
+               : launch_tc<true, false>(tq, tk, tv, tq, tq, p, grid, stream);
 }
 
 }  // namespace gqa
