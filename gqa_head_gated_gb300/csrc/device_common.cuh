@@ -60,9 +60,12 @@ __device__ __forceinline__ float2 unpack_elem2(uint32_t u) {
   if constexpr (kF16) return unpack_half2(u); else return unpack_bf16x2(u);
 }
 
-// Logistic function for the output gate, fp32.
+// Logistic function for the output gate, fp32.  The approximate divide has no
+// branch to an IEEE slow path, so a thread's 128 gates interleave; its error (a few
+// fp32 ulp, like __expf's) is far below the one rounding of the output to bf16/fp16.
+// g = -inf or < -88 gives exactly 0 (1/inf), g = +inf gives 1, NaN stays NaN.
 __device__ __forceinline__ float gate_sigmoid(float g) {
-  return 1.0f / (1.0f + __expf(-g));
+  return __fdividef(1.0f, 1.0f + __expf(-g));
 }
 
 }  // namespace gqa
