@@ -83,6 +83,10 @@ static_assert(kN == 64 || kN == 128, "key tile of 64 or 128");
 static_assert(kSlots * kTileBytes >= kQBytes, "the output tile is staged in the K/V ring");
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
+// General masks with one mask head for all query heads: the tile's mask rows (R query
+// rows x kN keys, each row padded by 16 bytes so that reads of different rows fall on
+// different banks) are staged in two slots behind the Smem block.
+constexpr int kMaskSlotBytes = 11264;
 constexpr uint32_t kTmO = 0;
 constexpr uint32_t kTmS = 256;                // S buffer b at kTmS + kN*b
 // Lazy-rescale threshold in log2 units: P <= 2^threshold must fit the element type
@@ -109,6 +113,8 @@ struct __align__(1024) Smem {
   uint64_t v_clean;            // split mode: the last V tile's padding rows are zeroed
   uint64_t q_free;             // prefill: every S product has read Q (its buffer takes G)
   uint64_t g_full;             // prefill: the gate tile has landed in Q's buffer
+  uint64_t mask_full[2];       // staged mask: slot holds tile j's mask rows
+  uint64_t mask_empty[2];      // staged mask: every softmax warp is done with the slot
   uint32_t tmem_base;
   int abort;
   int zero;
@@ -132,6 +138,7 @@ struct Params {
   const void* mask;
   int mask_kind, mask_hmode, mask_chunk, causal, Lkv;
   long long ms_b, ms_h, ms_i, ms_j;
+  int mask_stage;           // mask rows staged in shared memory (see kMaskSlotBytes)
   LaunchCtl ctl;
 };
 
@@ -224,8 +231,36 @@ __device__ __forceinline__ void apply_mask_row(uint32_t (&s)[kN_], const E* row,
   }
 }
 
+// The same for a row staged in shared memory (16-byte aligned, kN_ elements present,
+// zeros past the mask's last key).
+template <int kKind, typename E, int kN_>
+__device__ __forceinline__ void apply_mask_row_smem(uint32_t (&s)[kN_], const E* row, int key0,
+                                                    int lim) {
+  constexpr int kVec = 16 / int(sizeof(E));
+#pragma unroll
+  for (int c0 = 0; c0 < kN_; c0 += kVec) {
+    const uint4 u = *reinterpret_cast<const uint4*>(row + c0);
+    const E* e = reinterpret_cast<const E*>(&u);
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      if (key0 + c0 + v < lim) {
+        const float a = mask_elem<kKind>(e[v]);
+        const float x = __uint_as_float(s[c0 + v]);
+        s[c0 + v] = __float_as_uint(a == -INFINITY ? -INFINITY : fmaf(16.f, a, x));
+      }
+    }
+  }
+}
+
+static_assert(sizeof(Smem) + 1024 + 16 + 2 * kMaskSlotBytes <= 227 * 1024,
+              "the masked form's shared memory fits one CTA per SM");
+
+// Threads of a CTA: the general-mask form adds a warp that stages mask rows.
+template <bool kMask>
+constexpr int cta_threads() { return kMask ? kThreads + 32 : kThreads; }
+
 template <bool kSplit, bool kF16, bool kMask>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(cta_threads<kMask>(), 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                const __grid_constant__ CUtensorMap tmO, const Params p) {
@@ -307,6 +342,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     ptx::mbar_init(&sm.v_clean, 1);
     ptx::mbar_init(&sm.q_free, 1);
     ptx::mbar_init(&sm.g_full, 1);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      ptx::mbar_init(&sm.mask_full[s2], 32);   // the mask warp
+      ptx::mbar_init(&sm.mask_empty[s2], 8);   // the softmax warps
+    }
     sm.abort = 0;
     sm.zero = 0;
     ptx::fence_mbar_init();
@@ -489,6 +528,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       ptx::mbar_wait(&sm.drain, 0, tmo, &sm.zero);
     }
     __syncwarp();
+  } else if (warp >= kThreads / 32) {
+    // ------------------------------------------------------------ mask rows (kMask)
+    // With one mask head, the R query rows of the tile share their mask rows across
+    // the GQA heads: this warp copies tile j's rows into slot j % 2 (16-byte
+    // cp.async, zero past the mask's last key) while the softmax warps use slot
+    // (j - 1) % 2, and waits for the slot's release before reusing it.
+    if constexpr (kMask) {
+      if (p.mask_stage) {
+        const int es = p.mask_kind == 1 ? 1 : p.mask_kind == 2 ? 4 : 2;
+        const int pitch = kN * es + 16;
+        const int cpr = kN * es / 16;   // 16-byte chunks per row
+        const int kpc = 16 / es;        // keys per chunk
+        const char* mbase = static_cast<const char*>(p.mask);
+        uint8_t* const slots = reinterpret_cast<uint8_t*>(&sm) + ((sizeof(Smem) + 15) & ~size_t(15));
+        for (int j = 0; j < n_tiles; ++j) {
+          const int slot = j & 1;
+          if (j >= 2 &&
+              !warp_all(ptx::mbar_wait(&sm.mask_empty[slot], uint32_t((j - 2) >> 1) & 1u, tmo,
+                                       &sm.abort))) {
+            if (lane == 0) fail(sm, p);
+            break;
+          }
+          const int key0 = (j0 + j) * kN;
+          uint8_t* const dst = slots + slot * kMaskSlotBytes;
+          for (int c = lane; c < rows_here * cpr; c += 32) {
+            const int r = c / cpr, ch = c - r * cpr;
+            const int kf = key0 + ch * kpc;
+            const int nb = min(max((p.Lkv - kf) * es, 0), 16);
+            const char* src =
+                nb > 0 ? mbase + ((long long)b * p.ms_b + (long long)(r0 + r) * p.ms_i + kf) * es
+                       : mbase;
+            ptx::cp_async16(ptx::smem_addr(dst + r * pitch + ch * 16), src, uint32_t(nb));
+          }
+          ptx::cp_async_mbar_arrive(&sm.mask_full[slot]);
+        }
+        ptx::cp_async_wait_all();   // no copy may land after the CTA exits
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
     const int sw = warp - 2;
@@ -531,6 +608,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const int buf = j & 1;
       bool mine = warp_all(ptx::mbar_wait(&sm.s_full[buf], (j >> 1) & 1, tmo, &sm.abort)) &&
                   !sm.abort;
+      if constexpr (kMask) {
+        if (p.mask_stage)
+          mine = warp_all(ptx::mbar_wait(&sm.mask_full[buf], (j >> 1) & 1, tmo, &sm.abort)) &&
+                 mine;
+      }
       uint32_t s[kHalf];
       float mx = -INFINITY;
       if (mine) {
@@ -555,7 +637,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           }
         }
         if constexpr (kMask) {
-          if (valid && key0 < lim) {
+          if (p.mask_stage) {
+            if (valid && key0 < lim) {
+              const int es = p.mask_kind == 1 ? 1 : p.mask_kind == 2 ? 4 : 2;
+              const uint8_t* srow = reinterpret_cast<const uint8_t*>(&sm) +
+                                    ((sizeof(Smem) + 15) & ~size_t(15)) + buf * kMaskSlotBytes +
+                                    rr * (kN * es + 16) + half * kHalf * es;
+              switch (p.mask_kind) {
+                case 1:
+                  apply_mask_row_smem<1>(s, srow, key0, lim);
+                  break;
+                case 2:
+                  apply_mask_row_smem<2>(s, reinterpret_cast<const float*>(srow), key0, lim);
+                  break;
+                case 3:
+                  apply_mask_row_smem<3>(s, reinterpret_cast<const uint16_t*>(srow), key0, lim);
+                  break;
+                case 4:
+                  apply_mask_row_smem<4>(s, reinterpret_cast<const uint16_t*>(srow), key0, lim);
+                  break;
+                default:
+                  break;
+              }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.mask_empty[buf]);   // slot read by this warp
+          } else if (valid && key0 < lim) {
             switch (p.mask_kind) {
               case 1:
                 apply_mask_row<1>(s, static_cast<const uint8_t*>(p.mask) + mrow, p.ms_j, key0, lim);
@@ -780,12 +887,13 @@ template <bool kSplit, bool kF16, bool kMask = false>
 cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const CUtensorMap& tg, const CUtensorMap& to, const Params& p,
                       long long grid, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem) + 1024;
+  // the Smem block (1024-aligned), then for kMask the two mask slots
+  const size_t smem = sizeof(Smem) + 1024 + (kMask ? 16 + 2 * size_t(kMaskSlotBytes) : 0);
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kSplit, kF16, kMask>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<kSplit, kF16, kMask>
-      <<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tq, tk, tv, tg, to, p);
+  attn_tc_kernel<kSplit, kF16, kMask><<<dim3(unsigned(grid)), dim3(cta_threads<kMask>()), smem,
+                                        stream>>>(tq, tk, tv, tg, to, p);
   return cudaGetLastError();
 }
 
@@ -846,6 +954,16 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStrea
   p.ms_h = a.mask_strides[1];
   p.ms_i = a.mask_strides[2];
   p.ms_j = a.mask_strides[3];
+  {
+    // Stage the mask rows in shared memory when one mask head serves every query
+    // head, keys are contiguous and every staged row starts on a 16-byte boundary.
+    const int es = a.mask_kind == 1 ? 1 : a.mask_kind == 2 ? 4 : 2;
+    const bool aligned16 = reinterpret_cast<uintptr_t>(a.mask) % 16 == 0 &&
+                           (a.mask_strides[0] * es) % 16 == 0 && (a.mask_strides[2] * es) % 16 == 0;
+    p.mask_stage = (a.masked && a.mask_kind >= 1 && a.mask_kind <= 4 && a.mask_hmode == 0 &&
+                    a.mask_strides[3] == 1 && aligned16 && R * (kN * es + 16) <= kMaskSlotBytes)
+                       ? 1 : 0;
+  }
 
   const long long grid = (long long)p.n_rtiles * a.B * a.Hkv;
   if (a.masked)

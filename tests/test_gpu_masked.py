@@ -169,3 +169,29 @@ def test_masked_keys_with_nonfinite_k_are_ignored():
     x.k[:, 1, 105] = float("inf")
     b, _ = _run(x, m)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("mdtype", [torch.bool, torch.float32, torch.bfloat16, torch.float16])
+def test_staged_mask_rows_match_direct_loads(mdtype):
+    """A mask with one head whose rows start on 16-byte boundaries is staged in shared
+    memory by the kernel's mask warp (here a [Lq, 333] view of a [Lq, 352] tensor, so
+    the last 16-byte chunk of each row is partly past the mask); the same values in
+    rows that are not 16-byte aligned are read directly by the softmax threads. Both
+    match the oracle and each other bit for bit, causal and not."""
+    Lq, Lkv, wide = 190, 333, 352
+    x = _inputs(1, 24, 4, Lq, Lkv, seed=90)              # GQA 6: 21 query rows per tile
+    if mdtype == torch.bool:
+        base = torch.rand(Lq, wide, generator=_gen(90)) < 0.7
+    else:
+        base = torch.randn(Lq, wide, generator=_gen(90)) * 2
+        base[torch.rand(Lq, wide, generator=_gen(91)) < 0.15] = float("-inf")
+        base = base.to(mdtype)
+    staged = base[:, :Lkv]
+    odd = torch.empty(Lq, Lkv + 1, dtype=mdtype)[:, :Lkv]
+    odd.copy_(staged)
+    assert staged.stride(0) * staged.element_size() % 16 == 0
+    assert odd.stride(0) * odd.element_size() % 16 != 0
+    for causal in (False, True):
+        out_s, _ = _check(x, staged, f"staged {mdtype} causal={causal}", causal=causal)
+        out_d, _ = _run(x, odd, causal=causal)
+        assert torch.equal(out_s, out_d), f"staged vs direct {mdtype} causal={causal}"
