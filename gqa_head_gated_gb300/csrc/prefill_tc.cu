@@ -21,6 +21,8 @@
 //               and a pair of warps (w, w+4) shares its lanes: the first takes the
 //               first kN/2 keys of the tile, the second the rest; the two exchange
 //               row maxima and sums through shared memory.
+//   warp 10     general-mask form only (352 threads): stages the tile's mask rows
+//               in shared memory when one mask head serves all query heads.
 // TMEM (512 columns): O at 0..255 (fp32), S double buffer at 256 and 256 + kN;
 // P_j is written as bf16 pairs over the first kN/4 columns of each half of S_j.
 //
@@ -31,7 +33,8 @@
 // probability exactly 0 by selection, never exp(-inf)*0 arithmetic; K/V rows past
 // the last row's horizon are zero-filled by TMA, so nothing outside the visible
 // range is ever multiplied.
-// Epilogue: out = O / l * sigmoid(G), rounded once to bf16.
+// Epilogue: out = O / l * sigmoid(G), rounded once to bf16; the gate tile arrives by
+// TMA in Q's buffer and the output tile leaves by one TMA store from the K/V ring.
 //
 // Split mode (decode / chain verify, TensorFold PR #1009 "Receipt": decode over cache
 // chunks whose partial results are merged): one CTA takes R = floor(128/GQA) new
