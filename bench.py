@@ -841,6 +841,9 @@ CASES = {
     "verify_16k": lambda: S.make_decode(8, 16, 2, [1, 3, 4, 8, 16, 32, 1, 3],
                                         [4325, 854, 4593, 4238, 7757, 3758, 4011, 9102],
                                         Lcap=16384, seed=4),
+    # the prefill_4k inputs with an additive bf16 bias [4096, 4096] (N(0,2), seed 7,
+    # 32 MB) broadcast over heads, causal: the general-mask kernel, staged mask rows
+    "masked_4k": lambda: S.make_prefill(1, 24, 4, 4096, seed=2, outlier_frac=0.01),
 }
 
 
@@ -855,6 +858,14 @@ def run_case(name, launches, warmup):
         out = torch.empty_like(q)
         for _ in range(warmup + launches):
             G.prefill(q, k, v, g, kv_offset=x.kv_offset, out=out)
+    elif name.startswith("masked"):
+        q, k, v, g = (t.to(dev) for t in (x.q, x.k, x.v, x.g))
+        L = q.shape[2]
+        bias = (torch.randn(L, L, generator=torch.Generator().manual_seed(7)) * 2).to(
+            torch.bfloat16).to(dev)
+        out = torch.empty_like(q)
+        for _ in range(warmup + launches):
+            G.masked(q, k, v, g, bias, causal=True, kv_offset=0, out=out)
     else:
         q, kc, vc, g = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.g))
         kv, cu = x.kv_lens.to(dev), x.cu_rows.to(dev)
