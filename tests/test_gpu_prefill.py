@@ -44,6 +44,8 @@ CASES = [
     (1, 32, 1, 70, 100, 30),        # GQA 32 (4 rows per tile)
     (1, 128, 1, 5, 9, 3),           # GQA 128 (1 row per tile)
     (1, 8, 8, 640, 1000, 360),      # several K/V tiles, ragged everywhere
+    (2, 15, 3, 100, 100, 0),        # GQA 5: 25 rows x 5 heads = 125 packed rows per tile
+    (1, 21, 3, 77, 160, 83),        # GQA 7: 18 rows x 7 heads = 126, with an offset
 ]
 
 
