@@ -195,3 +195,17 @@ def test_staged_mask_rows_match_direct_loads(mdtype):
         out_s, _ = _check(x, staged, f"staged {mdtype} causal={causal}", causal=causal)
         out_d, _ = _run(x, odd, causal=causal)
         assert torch.equal(out_s, out_d), f"staged vs direct {mdtype} causal={causal}"
+
+
+def test_staged_masks_per_batch_and_key_padding():
+    """Staged mask rows with a batch stride: a per-batch [B,1,Lq,Lkv] bf16 bias and a
+    per-batch key-padding bool mask [B,1,1,Lkv] (row stride 0), both with 16-byte
+    aligned rows, against the oracle."""
+    B, Lq, Lkv = 2, 150, 272
+    x = _inputs(B, 16, 2, Lq, Lkv, seed=92)               # GQA 8: 16 query rows per tile
+    bias = (torch.randn(B, 1, Lq, Lkv, generator=_gen(92)) * 2).to(torch.bfloat16)
+    _check(x, bias, "per-batch staged bias", causal=True)
+    pad = torch.ones(B, 1, 1, Lkv, dtype=torch.bool)
+    pad[0, ..., 230:] = False
+    pad[1, ..., :7] = False
+    _check(x, pad, "staged key padding")
