@@ -169,3 +169,27 @@ def test_full_size_workloads_sampled(name):
     assert_parity(got, r_out, name)
     got_lse = np.array([float(lse[b, h, i]) for b, h, i in rows])
     np.testing.assert_allclose(got_lse, r_lse, rtol=0, atol=2e-3)
+
+
+def _random_shapes(n, seed):
+    """Seeded random prefill shapes: batch 1-2, 1-4 KV heads, GQA 1-12 (the third
+    page's 24 / 2 model among them), prompt 1-300 rows at an offset of 0-200."""
+    rng = np.random.default_rng(seed)
+    shapes = [(1, 24, 2, 97, 97 + 61, 61)]                 # GQA 12, 24 / 2 heads
+    while len(shapes) < n:
+        B = int(rng.integers(1, 3))
+        Hkv = int(rng.integers(1, 5))
+        gqa = int(rng.integers(1, 13))
+        Lq = int(rng.integers(1, 301))
+        off = int(rng.integers(0, 201))
+        shapes.append((B, Hkv * gqa, Hkv, Lq, Lq + off, off))
+    return shapes
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lkv,off", _random_shapes(10, 2024))
+def test_prefill_random_shapes(B, Hq, Hkv, Lq, Lkv, off):
+    x = S.make_prefill(B, Hq, Hkv, Lq, Lkv=Lkv, kv_offset=off, seed=Lq * 7 + Hq)
+    out, lse = run(x, lse=True)
+    r_out, r_lse = ref(x)
+    assert_parity(out, r_out, f"prefill random {B,Hq,Hkv,Lq,Lkv,off}")
+    np.testing.assert_allclose(to_f64(lse), r_lse, rtol=0, atol=2e-3)
