@@ -85,3 +85,42 @@ def test_tree_padding_never_read():
     x.v_cache[0, :, 1000:] = float("nan")
     b = run_tree(x, masks)
     assert torch.equal(a, b)
+
+
+def _random_verify(n, seed):
+    """Seeded random verify batches: 1-4 sequences of 0-40 new rows (0-64 for one of
+    them), GQA 1-12 over 1-4 KV heads, kv lengths from the rows up to 6,000; both
+    kernels are hit (the path follows max rows x GQA)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        Hkv = int(rng.integers(1, 5))
+        gqa = int(rng.integers(1, 13))
+        B = int(rng.integers(1, 5))
+        rows = [int(rng.integers(0, 41)) for _ in range(B)]
+        if rng.random() < 0.3:
+            rows[0] = int(rng.integers(41, 65))
+        if max(rows) == 0:
+            rows[0] = 1
+        kv = [r + int(rng.integers(0, 6001)) for r in rows]
+        kv = [max(k, 1) for k in kv]
+        out.append((Hkv * gqa, Hkv, rows, kv))
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv,rows,kv", _random_verify(8, 77) + [
+    (4, 2, [3, 9, 0, 5], [100, 5000, 0, 37]),        # mma.sync path, a sequence with no rows
+    (6, 3, [1, 1, 1], [1, 4097, 300])])               # decode rows, a one-key sequence
+def test_random_tree_and_chain_verify(Hq, Hkv, rows, kv):
+    x = S.make_decode(len(rows), Hq, Hkv, rows, kv, Lcap=max(kv) + 17, seed=sum(kv) + Hq)
+    masks = S.random_tree_masks(rows, sum(rows) + 5)
+    out, lse = run_tree(x, masks, lse=True)
+    r_out, r_lse = ref_tree(x, masks)
+    assert_parity(out, r_out, f"random tree {Hq, Hkv, rows, kv}")
+    np.testing.assert_allclose(to_f64(lse), r_lse, rtol=0, atol=2e-3)
+    chain = G.decode(x.q.to(DEV), x.k_cache.to(DEV), x.v_cache.to(DEV), x.g.to(DEV),
+                     x.kv_lens.to(DEV), x.cu_rows.to(DEV), max_rows=max(rows),
+                     max_kv_len=int(x.kv_lens.max()))
+    r_chain = oracle.decode(to_f64(x.q), to_f64(x.k_cache), to_f64(x.v_cache), to_f64(x.g),
+                            x.kv_lens.tolist(), x.cu_rows.tolist())[0]
+    assert_parity(chain, r_chain, f"random chain {Hq, Hkv, rows, kv}")
