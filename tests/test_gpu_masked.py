@@ -209,3 +209,41 @@ def test_staged_masks_per_batch_and_key_padding():
     pad[0, ..., 230:] = False
     pad[1, ..., :7] = False
     _check(x, pad, "staged key padding")
+
+
+def _random_masked(n, seed):
+    """Seeded random mask cases: broadcast shape, element type, causal rule and sizes
+    (key counts that do and do not give 16-byte aligned rows)."""
+    rng = np.random.default_rng(seed)
+    kinds = [torch.bool, torch.float32, torch.bfloat16, torch.float16]
+    shapes = ["2d", "1x1", "bx1", "full", "keypad"]
+    out = []
+    while len(out) < n:
+        Hkv = int(rng.integers(1, 4))
+        gqa = int(rng.integers(1, 9))
+        B = int(rng.integers(1, 3))
+        Lq = int(rng.integers(1, 200))
+        Lkv = Lq + int(rng.integers(0, 300))
+        if rng.random() < 0.5:
+            Lkv = max(16, (Lkv // 16) * 16)          # aligned rows for every element type
+            Lq = min(Lq, Lkv)
+        out.append((B, Hkv * gqa, Hkv, Lq, Lkv, shapes[int(rng.integers(len(shapes)))],
+                    kinds[int(rng.integers(len(kinds)))], bool(rng.random() < 0.5)))
+    return out
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lkv,shape,mdtype,causal", _random_masked(10, 314))
+def test_random_masks(B, Hq, Hkv, Lq, Lkv, shape, mdtype, causal):
+    x = _inputs(B, Hq, Hkv, Lq, Lkv, seed=Lq + Lkv + Hq)
+    dims = {"2d": (Lq, Lkv), "1x1": (1, 1, Lq, Lkv), "bx1": (B, 1, Lq, Lkv),
+            "full": (B, Hq, Lq, Lkv), "keypad": (B, 1, 1, Lkv)}[shape]
+    gen = _gen(Lq * 3 + Lkv)
+    if mdtype == torch.bool:
+        m = torch.rand(dims, generator=gen) < 0.8
+    else:
+        m = torch.randn(dims, generator=gen) * 2
+        m[torch.rand(dims, generator=gen) < 0.1] = float("-inf")
+        m = m.to(mdtype)
+    # a full-head mask is refused under head chunking (few rows, many heads per group)
+    _check(x, m, f"random mask {B, Hq, Hkv, Lq, Lkv, shape, mdtype, causal}", causal=causal,
+           chunking=shape != "full")
