@@ -34,7 +34,8 @@
 // the last row's horizon are zero-filled by TMA, so nothing outside the visible
 // range is ever multiplied.
 // Epilogue: out = O / l * sigmoid(G), rounded once to bf16; the gate tile arrives by
-// TMA in Q's buffer and the output tile leaves by one TMA store from the K/V ring.
+// TMA in Q's buffer and the output tile leaves by TMA stores from the K/V ring, half
+// of its column blocks while the other half is still being computed.
 //
 // Split mode (decode / chain verify, TensorFold PR #1009 "Receipt": decode over cache
 // chunks whose partial results are merged): one CTA takes R = floor(128/GQA) new
@@ -768,16 +769,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if constexpr (!kSplit) {
       if (p.G != nullptr) fin = warp_all(ptx::mbar_wait(&sm.g_full, 0, tmo, &sm.abort)) && fin;
     }
-    if (fin) {
-      ptx::tc_fence_after();
-      const float l_tot = l_part + sm.red[pb][half ^ 1][row];
-      // l_tot is 0 exactly when the row saw no key, NaN when it saw a NaN score.
-      const float inv_l = l_tot == 0.f ? 0.f : 1.f / l_tot;
-      if constexpr (!kSplit) {
-        const size_t row_off =
-            (size_t(b) * p.Hq + size_t(g * p.gqa + hh)) * size_t(p.Lq) + size_t(q);
+    const float l_tot = l_part + sm.red[pb][half ^ 1][row];
+    // l_tot is 0 exactly when the row saw no key, NaN when it saw a NaN score.
+    const float inv_l = l_tot == 0.f ? 0.f : 1.f / l_tot;
+    if constexpr (!kSplit) {
+      // Column blocks 0 and 2 are complete after the first two 32-column chunks of
+      // both row halves, blocks 1 and 3 after the last two: each pair is stored while
+      // the rest is computed (rows past Lq fall outside the tensor and are not
+      // written).  Every softmax thread takes both barriers, failed or not.
+      if (!fin) fail(sm, p);
+      if (fin) ptx::tc_fence_after();
+      const size_t row_off =
+          (size_t(b) * p.Hq + size_t(g * p.gqa + hh)) * size_t(p.Lq) + size_t(q);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
+        if (fin) {
           uint32_t o[32];
           ptx::tmem_ld32_wait(trow + kTmO + 128u * half + 32u * cc, o);
           const int dc = half * 2 + (cc >> 1);   // columns half*128 + cc*32 .. +31
@@ -805,45 +811,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             *reinterpret_cast<uint4*>(stage + off) = make_uint4(r[0], r[1], r[2], r[3]);
           }
         }
-        ptx::fence_proxy_async_smem();   // the staged tile is read by the TMA store
-        if (valid && half == 0 && p.lse != nullptr)
-          p.lse[row_off] = l_tot == 0.f ? -INFINITY : (m_run + __log2f(l_tot)) * kLn2;
-      } else {
-        // Normalised partial O / l (fp32) and lse for the merge; -inf: no key seen.
-        const size_t n = size_t(t0 + q) * p.Hq + size_t(g) * p.gqa + hh;
-        const size_t part = size_t(s_idx) * size_t(p.T) * p.Hq + n;
-        const bool live = valid && l_tot != 0.f;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t o[32];
-          ptx::tmem_ld32_wait(trow + kTmO + 128u * half + 32u * cc, o);
-          if (live) {
-            float4* op =
-                reinterpret_cast<float4*>(p.O_parts + part * kHeadDim + half * 128 + cc * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              op[v] = make_float4(
-                  __uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                  __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        if (cc & 1) {
+          if (fin) ptx::fence_proxy_async_smem();   // the staged blocks are read by TMA
+          ptx::named_bar_sync(5, 256);
+          if (threadIdx.x == 64 && *reinterpret_cast<volatile int*>(&sm.abort) == 0) {
+            const int d0 = cc >> 1, d1 = 2 + (cc >> 1);
+            ptx::tma_store_4d(&tmO, stage + d0 * kQChunk, d0 * 64, r0, g * p.gqa, b);
+            ptx::tma_store_4d(&tmO, stage + d1 * kQChunk, d1 * 64, r0, g * p.gqa, b);
+            ptx::bulk_commit_group();
           }
         }
-        if (valid && half == 0)
-          p.lse_parts[part] = live ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
       }
+      if (fin && valid && half == 0 && p.lse != nullptr)
+        p.lse[row_off] = l_tot == 0.f ? -INFINITY : (m_run + __log2f(l_tot)) * kLn2;
+      // Shared memory stays allocated until the stores have read it.
+      if (threadIdx.x == 64) ptx::bulk_wait_group_read0();
+    } else if (fin) {
+      ptx::tc_fence_after();
+      // Normalised partial O / l (fp32) and lse for the merge; -inf: no key seen.
+      const size_t n = size_t(t0 + q) * p.Hq + size_t(g) * p.gqa + hh;
+      const size_t part = size_t(s_idx) * size_t(p.T) * p.Hq + n;
+      const bool live = valid && l_tot != 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        ptx::tmem_ld32_wait(trow + kTmO + 128u * half + 32u * cc, o);
+        if (live) {
+          float4* op =
+              reinterpret_cast<float4*>(p.O_parts + part * kHeadDim + half * 128 + cc * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            op[v] = make_float4(
+                __uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+      }
+      if (valid && half == 0)
+        p.lse_parts[part] = live ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
     } else {
       fail(sm, p);
-    }
-    if constexpr (!kSplit) {
-      // Every softmax thread has staged its rows: one thread stores the tile (rows
-      // past Lq fall outside the tensor and are not written) and waits until the
-      // copy has read shared memory, which stays allocated until then.
-      ptx::named_bar_sync(5, 256);
-      if (threadIdx.x == 64 && *reinterpret_cast<volatile int*>(&sm.abort) == 0) {
-        for (int dc = 0; dc < 4; ++dc)
-          ptx::tma_store_4d(&tmO, stage + dc * kQChunk, dc * 64, r0, g * p.gqa, b);
-        ptx::bulk_commit_group();
-        ptx::bulk_wait_group_read0();
-      }
     }
   }
 
