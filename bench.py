@@ -560,6 +560,18 @@ def ours(args):
             "frac_of_bf16_peak": round(cp_flops / (cp_avg / 1e3) / 1e12 / float(peaks["bf16_tflops"]), 4),
             "avg_ms": round(cp_avg, 4)}
         del cp
+        # The 128-row prompt (24/4 heads): 28 CTAs, one key tile each, so it measures
+        # the kernel's latency, not its throughput.
+        tp = S.tiny_prefill()
+        tp_flops = prefill_flops(tp)
+        tp_ms = bench_prefill(tp, max(pf_steps, 20), max(3, args.warmup), dev, e2e=False)[0]
+        tp_avg = sum(tp_ms) / len(tp_ms)
+        more["tiny_prefill"] = {
+            "workload": "tiny prefill: B=1, Hq=24, Hkv=4, Lq=Lkv=128 causal, seed 0 "
+                        "(latency-bound: 28 CTAs of one key tile)",
+            "value": round(tp_flops / (tp_avg / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+            "avg_us": round(tp_avg * 1e3, 2)}
+        del tp
         vx = S.verify_35b()
         v_kv, v_bytes = decode_bytes(vx)
         vctx = setup_decode(vx, args.steps, dev, with_rows=True)
