@@ -65,18 +65,9 @@ namespace gqa {
 namespace {
 
 constexpr int kM = 128;                       // packed rows per tile
-#ifndef GQA_PF_KN
-#define GQA_PF_KN 128
-#endif
-#ifndef GQA_PF_KS
-#define GQA_PF_KS 1
-#endif
-#ifndef GQA_PF_VS
-#define GQA_PF_VS 1
-#endif
-constexpr int kN = GQA_PF_KN;                 // keys per K/V tile (64 or 128)
-constexpr int kKS = GQA_PF_KS;                // K ring slots (whole tiles)
-constexpr int kVS = GQA_PF_VS;                // V ring slots
+constexpr int kN = 128;                       // keys per K/V tile
+constexpr int kKS = 1;                        // K ring slots (whole tiles)
+constexpr int kVS = 1;                        // V ring slots
 constexpr int kSlots = kKS + kVS;
 constexpr int kQChunk = 128 * 128;            // Q: 128 rows x 64 bf16 per column block
 constexpr int kQBytes = 4 * kQChunk;
