@@ -11,7 +11,7 @@
 // and their O rows are never read.  A NaN lse (a part that saw a NaN score)
 // makes the row NaN, as float64 arithmetic of the formula would.  One warp per
 // row; each lane owns 8 of the 256 columns and reads them as two float4 per part,
-// the loads of eight parts issued together (the kernel is latency-bound: a decode
+// the loads of sixteen parts issued together (the kernel is latency-bound: a decode
 // merge moves a few MB).  It is launched as a programmatic dependent of the split
 // kernel, so its launch overlaps that kernel's last CTAs.
 #include <cuda_bf16.h>
@@ -31,7 +31,7 @@ __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-constexpr int kBatch = 8;   // parts whose loads are issued together
+constexpr int kBatch = 16;  // parts whose loads are issued together
 
 template <bool kF16>
 __global__ void __launch_bounds__(kWarps * 32)
