@@ -105,7 +105,9 @@ int gqa_attn_prefill(const void* Q, const void* K, const void* V, const void* G,
  * Kcache, Vcache: [B, Hkv, Lcap, 256] bf16.
  * kv_lens: int32 [B] (device): keys held for sequence b, counting its new rows;
  *   row i (0-based of r_b) sees keys j < kv_lens[b] - r_b + i + 1.  Cache rows at
- *   or beyond kv_lens[b] are never read (they may hold anything, NaN included).
+ *   or beyond kv_lens[b] never affect the result (they may hold anything, NaN
+ *   included): the mma.sync kernel does not read them, the tcgen05 kernel may copy
+ *   some into shared memory and clears them there before use.
  * cu_rows: int32 [B+1] (device) exclusive prefix sum of rows, or NULL for one row
  *   per sequence (then T must equal B and max_rows must be 1).
  * lse_out: NULL, or fp32 [T, Hq].
@@ -142,8 +144,10 @@ int gqa_attn_verify_tree(const void* Q, const void* Kcache, const void* Vcache, 
                          void* workspace, size_t workspace_bytes, gqa_stream_t stream);
 
 /*
- * The split plan gqa_attn_decode uses: the number of key splits S and the keys
- * per split (a multiple of 64).  Split s of sequence b covers keys
+ * The fixed split plan: the number of key splits S and the keys per split (a
+ * multiple of 64).  gqa_attn_decode uses it on the tcgen05 path and for B > 256;
+ * on the mma.sync path with B <= 256 it runs balanced shares with 16 part slots
+ * instead (see gqa_attn_decode_split).  Split s of sequence b covers keys
  * [s*split_keys, min((s+1)*split_keys, kv_lens[b])).  Host-only; returns
  * GQA_ERR_INVALID_ARG for bad sizes.
  */
