@@ -36,10 +36,11 @@ Readings where the pages are silent (each listed in the design notes):
   * tree verify: row i sees the keys before the new rows plus the new keys its
     mask selects (bit k = new row k); a chain is the mask of bits 0..i;
   * a row that sees no key outputs zeros and lse = -inf (float64 would give 0/0);
-  * keys a row does not see are excluded from its sums: the row's key range is
-    sliced, and inside a block of rows a key another row of the block sees gets
-    probability exactly 0 for this row (its V row is finite by the input contract,
-    since some row of the call sees it), so the sum is the excluded sum.
+  * keys a row does not see are excluded from its sums, never weighted by 0: each
+    row is evaluated on its own over exactly the keys it sees, so a NaN or Inf in
+    the K or V row of a key the row does not see cannot reach it (0 x Inf is NaN,
+    the hazard the TensorFold PR's second comment predicts for masked keys), and a
+    row's result does not depend on which other rows share the call.
 """
 from __future__ import annotations
 
@@ -49,7 +50,7 @@ import numpy as np
 
 HEAD_DIM = 256
 SCALE = 1.0 / 16.0          # 1/sqrt(head_dim)
-ROW_BLOCK = 256             # rows evaluated together; rows are independent
+ROW_BLOCK = 256             # rows handed to attend_rows at a time (each evaluated alone)
 
 
 def sigmoid(x):
@@ -75,34 +76,38 @@ def verify_visible(i: int, rows: int, kv_len: int) -> int:
 
 
 def attend_rows(q_rows, K, V, g_rows, lims):
-    """Gated attention of a block of query rows against one KV head.
+    """Gated attention of query rows against one KV head.
 
-    q_rows [n,D], g_rows [n,D] or None, K,V [L,D], lims [n] (keys each row sees).
+    q_rows [n,D], g_rows [n,D] or None, K,V [L,D], lims [n]: row i sees keys
+    0 .. lims[i]-1 and no other.  Every row is evaluated alone over the slice of
+    keys it sees (scores, max shift, sum and the weighted sum of V rows), so keys
+    past its limit take no part in any product for it.  Calling this with one row
+    or with that row inside a block gives the same bits.
     Returns (out [n,D], lse [n]) in float64.
     """
     q_rows = np.asarray(q_rows, dtype=np.float64)
-    lims = np.asarray(lims, dtype=np.int64)
+    lims = [int(x) for x in lims]
     n, D = q_rows.shape
     out = np.zeros((n, D))
     lse = np.full(n, -np.inf)
-    kmax = int(lims.max()) if n else 0
+    kmax = max(lims, default=0)
     if kmax <= 0:
         return out, lse
     Kb = np.asarray(K[:kmax], dtype=np.float64)
     Vb = np.asarray(V[:kmax], dtype=np.float64)
-    s = (q_rows @ Kb.T) * SCALE                      # [n, kmax]
-    seen = np.arange(kmax)[None, :] < lims[:, None]  # [n, kmax]
-    s = np.where(seen, s, -np.inf)
-    live = lims > 0
-    m = np.where(live, s.max(axis=1), 0.0)
-    p = np.where(seen, np.exp(s - m[:, None]), 0.0)
-    l = p.sum(axis=1)
-    o = np.zeros((n, D))
-    o[live] = (p[live] @ Vb) / l[live, None]
-    if g_rows is not None:
-        o = o * sigmoid(np.asarray(g_rows, dtype=np.float64))
-    out[live] = o[live]
-    lse[live] = m[live] + np.log(l[live])
+    for i in range(n):
+        lim = lims[i]
+        if lim <= 0:
+            continue                                  # sees no key: zeros, lse -inf
+        s = (Kb[:lim] @ q_rows[i]) * SCALE            # scores of the visible keys
+        m = np.max(s)
+        p = np.exp(s - m)
+        l = np.sum(p)
+        o = (p @ Vb[:lim]) / l
+        if g_rows is not None:
+            o = o * sigmoid(np.asarray(g_rows[i], dtype=np.float64))
+        out[i] = o
+        lse[i] = m + math.log(l)                      # l >= 1, or NaN
     return out, lse
 
 

@@ -19,15 +19,14 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 MUTANTS = {
     "one key too far (prefill)": ("return kv_offset + i + 1", "return kv_offset + i + 2"),
     "one key too far (verify)": ("return kv_len - rows + i + 1", "return kv_len - rows + i + 2"),
-    "one key short (mask compare)": ("np.arange(kmax)[None, :] < lims[:, None]",
-                                     "np.arange(kmax)[None, :] < lims[:, None] - 1"),
+    "one key short (row limit)": ("        lim = lims[i]\n", "        lim = lims[i] - 1\n"),
     "wrong scale": ("SCALE = 1.0 / 16.0", "SCALE = 1.0 / 8.0"),
     "interleaved kv heads": ("return h // (Hq // Hkv)", "return h % Hkv"),
-    "transposed operand (V for K)": ("s = (q_rows @ Kb.T) * SCALE", "s = (q_rows @ Vb.T) * SCALE"),
-    "dropped normalisation": ("o[live] = (p[live] @ Vb) / l[live, None]", "o[live] = (p[live] @ Vb)"),
-    "dropped max shift": ("m = np.where(live, s.max(axis=1), 0.0)", "m = np.where(live, 0.0 * s.max(axis=1), 0.0)"),
+    "transposed operand (V for K)": ("s = (Kb[:lim] @ q_rows[i]) * SCALE", "s = (Vb[:lim] @ q_rows[i]) * SCALE"),
+    "dropped normalisation": ("o = (p @ Vb[:lim]) / l", "o = (p @ Vb[:lim])"),
+    "dropped max shift": ("m = np.max(s)", "m = 0.0 * np.max(s)"),
     "gate sign": ("return 1.0 / (1.0 + np.exp(-x))", "return 1.0 / (1.0 + np.exp(x))"),
-    "lse without ln l": ("lse[live] = m[live] + np.log(l[live])", "lse[live] = m[live]"),
+    "lse without ln l": ("lse[i] = m + math.log(l)", "lse[i] = m"),
     "merge drops last part": ("live = [s for s in range(S) if lse_parts[s, n] != -np.inf]",
                               "live = [s for s in range(S) if lse_parts[s, n] != -np.inf][:-1]"),
     "merge skips NaN parts": ("live = [s for s in range(S) if lse_parts[s, n] != -np.inf]",
@@ -43,8 +42,12 @@ MUTANTS = {
     "mask: causal one key too far": ("np.arange(Lkv)[None, :] <= kv_offset + np.arange(Lq)[:, None]",
                                      "np.arange(Lkv)[None, :] <= kv_offset + 1 + np.arange(Lq)[:, None]"),
     "mask: -inf bias kept": ("                    keep = base & (a != -np.inf)", "                    keep = base"),
-    "scores without NaN": ("s = np.where(seen, s, -np.inf)",
-                           "s = np.where(seen & ~np.isnan(s), s, -np.inf)"),
+    "scores without NaN": ("        m = np.max(s)\n",
+                           "        s = np.where(np.isnan(s), -np.inf, s)\n        m = np.max(s)\n"),
+    # keys a row does not see weighted by probability 0 instead of excluded: a NaN or
+    # Inf in their V rows then reaches the row (0 x Inf = NaN)
+    "masked V multiplied by 0": ("o = (p @ Vb[:lim]) / l",
+                                 "o = (np.concatenate([p, np.zeros(kmax - lim)]) @ Vb) / l"),
     "merge ignores weights": ("acc += ws * O_parts[s, n]", "acc += O_parts[s, n]"),
     "plan drops remainder": ("    if gqa % c:\n        plan.append(gqa % c)\n", ""),
     "tree: new rows start one key late": ("    base = kv_len - rows\n    return list(range(base))",

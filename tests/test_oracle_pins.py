@@ -17,8 +17,11 @@
   query row is NaN, an Inf value under a positive probability is Inf in that
   column only, an Inf score poisons exactly the rows whose score is +Inf and
   drops the key where it is -Inf (checked by brute force over the other keys),
-  a -Inf gate gives 0, a NaN merge part gives a NaN row, and non-finite values
-  in positions no row sees change nothing;
+  a -Inf gate gives 0, a NaN merge part gives a NaN row, non-finite values
+  in positions no row sees change nothing, and non-finite K/V of a key that
+  earlier rows of the call do not see and later rows do leave the earlier rows
+  bitwise unchanged (excluded, not weighted by 0) while the later rows carry the
+  IEEE result;
 * general masks: brute force over the kept keys (bool) and with exact biases
   (additive), torch's scaled_dot_product_attention with bool and float masks,
   2-D == expanded 4-D, all-True + causal == prefill, additive -inf == False, a
@@ -548,6 +551,98 @@ def check_nonfinite_unseen(ora):
     return "" if np.array_equal(c, e) and np.isfinite(c).all() else "cache padding changed a row"
 
 
+def _expect_rows(a, la, b, lb, spec, what):
+    """Row-by-row comparison of a planted run (b, lb) with the clean run (a, la).
+    spec(idx) is None (the row and its lse are bitwise unchanged), "nan" (out and
+    lse NaN), or {column: "nan" | "+inf" | "-inf"} (those columns so, every other
+    column and the lse bitwise unchanged)."""
+    kinds = {"nan": np.isnan, "+inf": lambda v: v == np.inf, "-inf": lambda v: v == -np.inf}
+    for idx in np.ndindex(*la.shape):
+        want = spec(idx)
+        if want is None:
+            if not (np.array_equal(a[idx], b[idx]) and la[idx] == lb[idx]):
+                return f"{what}: row {idx} changed by a key it does not see"
+        elif want == "nan":
+            if not (np.isnan(b[idx]).all() and np.isnan(lb[idx])):
+                return f"{what}: row {idx} is not NaN"
+        else:
+            for c, kind in want.items():
+                if not kinds[kind](b[idx][c]):
+                    return f"{what}: row {idx} column {c} is {b[idx][c]}, want {kind}"
+            rest = np.ones(a.shape[-1], bool)
+            rest[list(want)] = False
+            if not (np.array_equal(a[idx][rest], b[idx][rest]) and la[idx] == lb[idx]):
+                return f"{what}: row {idx} changed outside the planted columns"
+    return ""
+
+
+def check_nonfinite_masked_kv(ora):
+    """NaN, +Inf and -Inf in the V rows (and NaN in a K row) of keys that earlier
+    rows of the same call do not see and later rows do, in a prompt chunk at an
+    offset and in a chain-verify block.  Keys a row does not see are excluded from
+    its sums, so that row equals the clean run bit for bit (a probability-0
+    product would make it NaN); a row that sees a planted V value is NaN / +Inf /
+    -Inf in exactly that column (probability > 0, gate > 0) and bitwise unchanged
+    elsewhere; a row that sees the NaN key is NaN.  Every row evaluated alone
+    (rows=) gives the block evaluation's bits."""
+    x = make_prefill(1, 4, 2, 6, Lkv=9, kv_offset=3, seed=47)
+    Q, K, V, G = (f64(t) for t in (x.q, x.k, x.v, x.g))
+    a, la = ora.prefill(Q, K, V, G, 3)            # row i sees keys 0 .. 3 + i
+    V[0, 0, 5, 7] = np.nan                        # KV head 0: key 5 seen by rows 2..5
+    V[0, 0, 6, 8] = np.inf                        # key 6: rows 3..5
+    V[0, 0, 8, 9] = -np.inf                       # key 8: row 5 only
+    V[0, 1, 4, 10] = np.inf                       # KV head 1: key 4 seen by rows 1..5
+    K[0, 1, 7, 3] = np.nan                        # key 7: rows 4, 5 score NaN
+    b, lb = ora.prefill(Q, K, V, G, 3)
+
+    def pre_spec(idx):
+        _, h, i = idx
+        if h < 2:
+            cols = {c: k for c, k, first in ((7, "nan", 2), (8, "+inf", 3), (9, "-inf", 5))
+                    if i >= first}
+            return cols or None
+        if i >= 4:
+            return "nan"
+        return {10: "+inf"} if i >= 1 else None
+
+    e = _expect_rows(a, la, b, lb, pre_spec, "prefill chunk")
+    if e:
+        return e
+    rows = [(0, h, i) for h in range(4) for i in range(6)]
+    c, lc = ora.prefill(Q, K, V, G, 3, rows=rows)
+    for n, idx in enumerate(rows):
+        if not (np.array_equal(c[n], b[idx], equal_nan=True) and
+                np.array_equal(lc[n], lb[idx], equal_nan=True)):
+            return f"prefill row {idx} alone differs from the block"
+
+    y = make_decode(1, 4, 2, rows=[4], kv_lens=[9], Lcap=10, seed=48, pad_value=0.0)
+    Qd, Kd, Vd, Gd = (f64(t) for t in (y.q, y.k_cache, y.v_cache, y.g))
+    a, la = ora.decode(Qd, Kd, Vd, Gd, [9], [0, 4])   # row t sees keys 0 .. 5 + t
+    Vd[0, 0, 6, 20] = -np.inf                     # KV head 0: key 6 seen by rows 1..3
+    Kd[0, 0, 7, 30] = np.nan                      # key 7: rows 2, 3 score NaN
+    Vd[0, 1, 7, 22] = np.inf                      # KV head 1: key 7 seen by rows 2, 3
+    Vd[0, 1, 8, 21] = np.nan                      # key 8: row 3 only
+    b, lb = ora.decode(Qd, Kd, Vd, Gd, [9], [0, 4])
+
+    def dec_spec(idx):
+        t, h = idx
+        if h < 2:
+            return None if t == 0 else {20: "-inf"} if t == 1 else "nan"
+        cols = {c: k for c, k, first in ((22, "+inf", 2), (21, "nan", 3)) if t >= first}
+        return cols or None
+
+    e = _expect_rows(a, la, b, lb, dec_spec, "chain verify")
+    if e:
+        return e
+    rows = [(t, h) for t in range(4) for h in range(4)]
+    c, lc = ora.decode(Qd, Kd, Vd, Gd, [9], [0, 4], rows=rows)
+    for n, idx in enumerate(rows):
+        if not (np.array_equal(c[n], b[idx], equal_nan=True) and
+                np.array_equal(lc[n], lb[idx], equal_nan=True)):
+            return f"verify row {idx} alone differs from the block"
+    return ""
+
+
 def check_nonfinite_merge(ora):
     """A NaN part makes its row NaN (out and lse); a -inf part with NaN O is not
     read; +Inf lse gives NaN (exp(Inf - Inf))."""
@@ -737,7 +832,8 @@ CHECKS = [
     check_merge_empty_row, check_plan_golden, check_brute_tree, check_tree_chain_is_decode,
     check_tree_storage_permutation, check_kv_append_brute, check_kv_keep_brute,
     check_append_then_chain_verify, check_nonfinite_q_row, check_nonfinite_v_column,
-    check_nonfinite_k_sign, check_nonfinite_k_nan, check_nonfinite_gate, check_nonfinite_unseen, check_nonfinite_merge,
+    check_nonfinite_k_sign, check_nonfinite_k_nan, check_nonfinite_gate, check_nonfinite_unseen,
+    check_nonfinite_masked_kv, check_nonfinite_merge,
     check_masked_brute_bool, check_masked_brute_additive, check_masked_library_sdpa,
     check_masked_reductions, check_masked_chunk_local, check_mask_rules_golden,
 ]
