@@ -24,6 +24,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace gqa {
@@ -114,6 +116,67 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// ---------------------------------------------------------------- non-finite V values
+// Keys that some rows of a block see and others do not ([pr_lo, pr_hi), fewer than 64)
+// meet probability 0 in the P.V product for the rows that do not see them.  Their V
+// rows' NaN / Inf elements are set to 0 in shared memory before the product and added
+// back, as p * V, for the rows that see them when the part is written (keys a row does
+// not see are excluded from its sums, never weighted by 0).  These helpers stay out of
+// line so that the kernel's steady-state code is as it is without them.
+
+// All threads: clears the NaN / Inf elements of V rows r_lo .. r_lo+nr-1 of a tile and
+// sets bit (tile key0 + r - pr_lo) of *hit for each row that held one.
+template <bool kF16>
+__device__ __noinline__ void clean_tile_rows(uint8_t* vt, int r_lo, int nr, int bit0,
+                                             unsigned long long* hit) {
+  for (int c = threadIdx.x; c < nr * 32; c += blockDim.x) {
+    const int r = r_lo + (c >> 5);
+    uint4* const a = reinterpret_cast<uint4*>(vt + uint32_t(r) * 512u +
+                                              uint32_t(((c & 31) ^ (r & 7)) << 4));
+    uint4 u = *a;
+    if (clear_nonfinite<kF16>(u)) {
+      *a = u;
+      atomicOr(hit, 1ull << (bit0 + r));
+    }
+  }
+}
+
+// Records bit off of *pz for each hit key this thread holds a zero probability for:
+// z bit (2 * nt + e) = probability 0 for key key_w + 8 nt + 2 t4 + e.
+__device__ __noinline__ void record_zero_probs(unsigned long long* pz, unsigned long long hits,
+                                               int first_off, int t4, uint32_t z, int nt_count) {
+  for (int nt = 0; nt < nt_count; ++nt)
+    for (int e = 0; e < 2; ++e) {
+      const int off = first_off + nt * 8 + 2 * t4 + e;
+      if (((z >> (2 * nt + e)) & 1u) && off >= 0 && off < 64 && ((hits >> off) & 1ull))
+        atomicOr(pz, 1ull << off);
+    }
+}
+
+// p * V of the NaN / Inf elements taken out of P.V, for the hit keys a row sees, added
+// to its normalised part (4 columns at Vg_c; a NaN or an infinity, so the scale of p
+// does not matter; p = 0 gives NaN as float64 would).
+template <bool kF16>
+__device__ __noinline__ float4 add_hit_terms(float4 acc, unsigned long long hits,
+                                             unsigned long long pz, int pr_lo, int lim,
+                                             bool tree, int base, unsigned long long msk,
+                                             const uint16_t* Vg_c) {
+  while (hits != 0ull) {
+    const int off = __ffsll(static_cast<long long>(hits)) - 1;
+    hits &= hits - 1ull;
+    const int key = pr_lo + off;
+    if (key >= lim || (tree && key >= base && !((msk >> (key - base)) & 1ull))) continue;
+    const float keep = ((pz >> off) & 1ull) ? 0.f : 1.f;
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(Vg_c + size_t(key) * 256));
+    const uint32_t x[4] = {u.x & 0xFFFFu, u.x >> 16, u.y & 0xFFFFu, u.y >> 16};
+    float* const a = &acc.x;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (elem_nonfinite<kF16>(x[e])) a[e] += keep * elem_to_float<kF16>(x[e]);
+  }
+  return acc;
+}
+
 // WR row groups of 16 packed rows; WK key groups per row group (WR * WK warps).
 template <int WR, int WK, bool kF16>
 __global__ void __launch_bounds__(kThreads)
@@ -131,6 +194,11 @@ decode_split_kernel(const Params p) {
   __shared__ float s_l[WK][MB];
   __shared__ int s_lim[MB];
   __shared__ unsigned long long s_mask[MB];
+  // Keys some rows of the block see and others do not, [pr_lo, pr_hi) (fewer than 64):
+  // bit k of s_hit = key pr_lo + k had a NaN / Inf V element (set to 0 in shared
+  // memory before P.V); bit k of s_pz[row] = the row's probability for that key was 0.
+  __shared__ unsigned long long s_hit;
+  __shared__ unsigned long long s_pz[MB];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -177,13 +245,20 @@ decode_split_kernel(const Params p) {
     }
     s_lim[tid] = min(lim, k_hi);
     s_mask[tid] = m;
+    s_pz[tid] = 0ull;
   }
+  if (tid == 0) s_hit = 0ull;
   int n_hi = 0;   // keys any row of the block sees in this split
   {
     const int pl = min(P - 1, p0 + MB - 1);
     n_hi = min(tree ? kv_len : base + pl / p.gqa + 1, k_hi);
   }
+  // Chain: the block's first row sees keys < base + p0/gqa + 1, so later new keys are
+  // seen by some rows only; tree: any new key may be.
+  const int pr_lo = max(k_lo, tree ? base : base + p0 / p.gqa + 1);
+  const int pr_hi = n_hi;
   const int n_tiles = n_hi > k_lo ? (n_hi - k_lo + kTK - 1) / kTK : 0;
+  const int scan_from = pr_hi > pr_lo ? (pr_lo - k_lo) / kTK : n_tiles;   // first tile to clean
 
   const size_t kv_base = (size_t(b) * p.Hkv + g) * size_t(p.Lcap) * 256;
   const uint16_t* Kg = p.K + kv_base;
@@ -236,7 +311,10 @@ decode_split_kernel(const Params p) {
   float m_r[2] = {-INFINITY, -INFINITY};
   float l_r[2] = {0.f, 0.f};
 
-  for (int tile = 0; tile < n_tiles; ++tile) {
+  // One tile of keys; the tiles from scan_from on (keys some rows of the block do not
+  // see) also get their V rows cleaned, in a second instance of the step so that the
+  // steady-state loop carries none of that.
+  auto step = [&](const int tile, auto with_hits) {
     cp_async_wait<kStages - 2>();
     __syncthreads();
     {
@@ -244,8 +322,22 @@ decode_split_kernel(const Params p) {
       if (nt < n_tiles) load_tile(nt, nt % kStages);
       cp_async_commit();
     }
-    if (!compute) continue;
     const int stage = tile % kStages;
+    // Keys of this tile that some rows do not see: their V rows' NaN / Inf elements are
+    // set to 0 here, so a row that does not see the key multiplies 0 (not Inf or NaN)
+    // by its probability 0; the rows that see it get p * V of the original element
+    // added when the part is written (keys a row does not see are excluded from its
+    // sums, never weighted by 0).
+    bool hit_tile = false;
+    if constexpr (decltype(with_hits)::value) {
+      const int tkey0 = k_lo + tile * kTK;
+      const int r_lo = max(pr_lo - tkey0, 0);
+      clean_tile_rows<kF16>(sKV + stage * 2 * kTileBytes + kTileBytes, r_lo,
+                            min(pr_hi - tkey0, kTK) - r_lo, tkey0 - pr_lo, &s_hit);
+      __syncthreads();
+      hit_tile = s_hit != 0ull;
+    }
+    if (!compute) return;
     const uint32_t kb = saddr(sKV + stage * 2 * kTileBytes);
     const uint32_t vb = kb + kTileBytes;
     const uint32_t qb = saddr(sQ);
@@ -321,6 +413,15 @@ decode_split_kernel(const Params p) {
           ls += pv;
         }
       }
+      if (decltype(with_hits)::value && hit_tile) {
+        // record the hit keys this row's probability is 0 for
+        uint32_t z = 0u;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) z |= uint32_t(sc[nt][2 * hr + e] == 0.f) << (2 * nt + e);
+        record_zero_probs(&s_pz[wr * 16 + g4 + 8 * hr], s_hit, key_w - pr_lo, t4, z, NT);
+      }
       l_r[hr] = l_r[hr] * alpha + ls;
 #pragma unroll
       for (int dn = 0; dn < 32; ++dn) {
@@ -345,7 +446,9 @@ decode_split_kernel(const Params p) {
         mma_16b<kF16>(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
       }
     }
-  }
+  };
+  for (int tile = 0; tile < min(scan_from, n_tiles); ++tile) step(tile, std::false_type{});
+  for (int tile = scan_from; tile < n_tiles; ++tile) step(tile, std::true_type{});
   cp_async_wait<0>();
   __syncthreads();
 
@@ -404,6 +507,9 @@ decode_split_kernel(const Params p) {
     acc.y *= inv;
     acc.z *= inv;
     acc.w *= inv;
+    if (s_hit != 0ull)
+      acc = add_hit_terms<kF16>(acc, s_hit, s_pz[r], pr_lo, s_lim[r], tree, base, s_mask[r],
+                                Vg + c4);
     *reinterpret_cast<float4*>(p.O_parts + part * 256 + c4) = acc;
     if (c4 == 0) p.lse_parts[part] = (Msub + __log2f(L)) * kLn2;
   }

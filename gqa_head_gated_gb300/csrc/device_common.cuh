@@ -60,6 +60,49 @@ __device__ __forceinline__ float2 unpack_elem2(uint32_t u) {
   if constexpr (kF16) return unpack_half2(u); else return unpack_bf16x2(u);
 }
 
+// Non-finite V values at keys masked for some rows (both kernels).
+// A 16-bit element (bf16 or fp16 bits) that is NaN or +-Inf: exponent all ones.
+template <bool kF16>
+__device__ __forceinline__ bool elem_nonfinite(uint32_t e) {
+  return kF16 ? (e & 0x7C00u) == 0x7C00u : (e & 0x7F80u) == 0x7F80u;
+}
+template <bool kF16>
+__device__ __forceinline__ float elem_to_float(uint32_t e) {
+  if constexpr (kF16) return __half2float(__ushort_as_half(static_cast<unsigned short>(e)));
+  else return __uint_as_float(e << 16);
+}
+// Sets the NaN / Inf elements of a 16-byte chunk to +0; returns whether there was one.
+template <bool kF16>
+__device__ __forceinline__ bool clear_nonfinite(uint4& u) {
+  uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  bool any = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (elem_nonfinite<kF16>(w[i] & 0xFFFFu)) { w[i] &= 0xFFFF0000u; any = true; }
+    if (elem_nonfinite<kF16>(w[i] >> 16)) { w[i] &= 0x0000FFFFu; any = true; }
+  }
+  u = make_uint4(w[0], w[1], w[2], w[3]);
+  return any;
+}
+
+// acc + x * 0 on a packed pair (acc starts at +0): stays +0 while every x is finite and
+// becomes NaN for good once some x is NaN or +-Inf (Inf * 0 is NaN).
+template <bool kF16>
+__device__ __forceinline__ uint32_t nonfinite_acc(uint32_t acc, uint32_t x) {
+  uint32_t r;
+  if constexpr (kF16)
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0u), "r"(acc));
+  else
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0u), "r"(acc));
+  return r;
+}
+// The same for one fp32 value.
+__device__ __forceinline__ float nonfinite_acc_f32(float acc, float x) {
+  float r;
+  asm("fma.rn.f32 %0, %1, 0f00000000, %2;" : "=f"(r) : "f"(x), "f"(acc));
+  return r;
+}
+
 // Logistic function for the output gate, fp32.  The approximate divide has no
 // branch to an IEEE slow path, so a thread's 128 gates interleave; its error (a few
 // fp32 ulp, like __expf's) is far below the one rounding of the output to bf16/fp16.

@@ -27,15 +27,21 @@
  *   - lse outputs, when requested, are fp32 natural-log sum-exp of the scaled
  *     scores over the keys a row sees (-inf for a row that sees no key).
  *   - A row that sees no key outputs zeros.
- *   - Non-finite inputs: NaN or +-Inf in positions no row of the call sees
- *     (cache rows at or past kv_len, keys after the last prompt row) never change
- *     an output, and neither do non-finite K values of keys masked for a row.
- *     Non-finite Q, G, and K/V of keys that every row of the call sees propagate
+ *   - Non-finite inputs: a key a row does not see is excluded from that row's
+ *     sums, never weighted by probability 0.  So NaN or +-Inf anywhere in the K
+ *     or V row of such a key (cache rows at or past kv_len, keys after the last
+ *     prompt row, keys the causal rule, a tree mask or a general mask hides from
+ *     the row while other rows of the call see them) never changes that row's
+ *     output, bit for bit.  Non-finite Q, G, and K/V of keys a row sees propagate
  *     as IEEE float64 arithmetic of the formula would: a NaN score or value gives
  *     NaN, an Inf value under a positive probability gives +-Inf, a -Inf gate
- *     gives 0.  A non-finite V row masked for some rows of a call but seen by
- *     others may turn the masked rows' outputs NaN: they multiply it by
- *     probability 0 inside the tensor-core product, and 0 * Inf is NaN.
+ *     gives 0.  Finite inputs pay one check of each tile's outputs; a tile whose
+ *     outputs hold a NaN / Inf is computed again with the non-finite V elements
+ *     of keys some of its rows do not see taken out of the tensor-core product
+ *     and added back for the rows that see them.  Limit: the general-mask calls
+ *     handle up to 256 keys with a non-finite V element per tile of query rows
+ *     and KV head (every other call: any number); past that, rows that do not
+ *     see the further keys may read NaN.
  *   - Ownership: the caller owns every buffer.  The library never allocates
  *     device memory; the decode workspace is caller-provided.
  *   - Streams: every call is asynchronous on `stream` (may be 0 = legacy default
