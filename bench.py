@@ -274,6 +274,29 @@ def oracle_decode_sample(x, budget_s=10.0, min_seqs=1):
 DECODE_WORKLOAD = ("27B-shape decode: B=16, Hq=24, Hkv=4, head_dim=256, 1 row/seq, kv_lens "
                    "uniform [1024,32768] (sum 297,628), cache [16,4,32768,256] bf16, seed 1")
 BAL_PARTS = 16     # part slots per row of the one-call decode's balanced shares
+def last_launch(prefix):
+    """The library's record (gqa_launch_log) of its newest launch of a kernel whose
+    name starts with `prefix`: grid, block and dynamic shared memory as launched."""
+    import gqa_head_gated_gb300 as G
+    for r in G.launch_log():
+        if r["kernel"].startswith(prefix):
+            return {"kernel": r["kernel"], "grid": r["grid"], "block": r["block"],
+                    "dynamic_smem_bytes": r["dynamic_smem"], "source": "gqa_launch_log"}
+    return None
+
+
+def decode_config(x):
+    """The `config` both arms print (the workload and how it is timed)."""
+    kv_bytes, step_bytes = decode_bytes(x)
+    return {"workload": DECODE_WORKLOAD,
+            "bytes_per_step": step_bytes,
+            "kv_bytes_per_step": kv_bytes,
+            "l2": "GPU arm: flushed before every timed step (256 MiB write, outside the "
+                  "events); reference arm: host cores",
+            "parallelism": "one replica per GPU, no data-path collective; reference arm: "
+                           "rank 0 on the host cores"}
+
+
 def setup_decode(x, steps, dev, with_rows=False):
     """Device copies and the split plan of a decode (one row per sequence) or, with
     `with_rows`, a verify workload (cu_rows passed to the kernels)."""
@@ -293,18 +316,21 @@ def setup_decode(x, steps, dev, with_rows=False):
                 plan=(S_, C_), ev=ev, ws=ws, out=torch.empty_like(q), flush=L2Flush(dev))
 
 
-def run_decode_timed(ctx, steps, tree_mask=None):
+def run_decode_timed(ctx, steps, tree_mask=None, noalloc=False):
     """One decode step = one gqa_attn_decode call (gqa_attn_verify_tree with a tree
-    mask): the split kernel, then the merge launched as its programmatic dependent.
-    Bracketed by events on the launching (current) stream; L2 flushed before each
-    step, outside the events."""
+    mask, gqa_attn_decode_noalloc with `noalloc`): the split kernel, then the merge
+    launched as its programmatic dependent.  Bracketed by events on the launching
+    (current) stream; L2 flushed before each step, outside the events."""
     import gqa_head_gated_gb300 as G
     q, kc, vc, kv, g = ctx["q"], ctx["kc"], ctx["vc"], ctx["kv"], ctx["g"]
     for i in range(steps):
         ctx["flush"]()
         a, b = ctx["ev"][i % len(ctx["ev"])]
         a.record()
-        if tree_mask is None:
+        if noalloc:
+            G.decode_noalloc(q, kc, vc, g, kv, ctx["cu"], max_rows=ctx["max_rows"],
+                             max_kv_len=ctx["max_kv"], out=ctx["out"])
+        elif tree_mask is None:
             G.decode(q, kc, vc, g, kv, ctx["cu"], max_rows=ctx["max_rows"],
                      max_kv_len=ctx["max_kv"], workspace=ctx["ws"], out=ctx["out"])
         else:
@@ -479,9 +505,11 @@ def ours(args):
 
     barrier(world)
     torch.cuda.synchronize()
+    seq0 = G.launch_log(1)[0]["seq"]
     with ClockSampler(local) as clk:
         run_decode_timed(ctx, args.steps)
         torch.cuda.synchronize()
+    launches = G.launch_log(1)[0]["seq"] - seq0    # the library's launches in the timed region
     barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in ctx["ev"]]
     total_ms = max_over_ranks(world, sum(step_ms))
@@ -503,6 +531,7 @@ def ours(args):
         if i >= args.warmup:
             split_ms.append(a.elapsed_time(b))
     del op, lp
+    split_launch = last_launch("decode_split_kernel")
     status = G.last_device_status()
     out_ok = bool(torch.isfinite(ctx["out"].float()).all().item())
 
@@ -529,6 +558,7 @@ def ours(args):
     pf_steps = max(3, min(args.steps, 10))
     pf_ms, pf_status, pf_e2e, pf_h2d, pf_d2h, pf_clk = bench_prefill(pf, pf_steps,
                                                                      max(3, args.warmup), dev)
+    pf_launch = last_launch("attn_tc_kernel<prefill")
     pf_avg = sum(pf_ms) / len(pf_ms)
     pf_tflops = flops / (pf_avg / 1e3) / 1e12
     bf16_peak = float(peaks["bf16_tflops"])
@@ -648,6 +678,24 @@ def ours(args):
             "ms_per_step": round(f_step, 5), "outputs_finite": f_ok}
         del fctx, xf
         torch.cuda.empty_cache()
+        # the headline decode through gqa_attn_decode_noalloc (the library's fixed area
+        # as workspace; same kernels and plan)
+        nctx = setup_decode(x, args.steps, dev)
+        run_decode_timed(nctx, args.warmup, noalloc=True)
+        torch.cuda.synchronize()
+        run_decode_timed(nctx, args.steps, noalloc=True)
+        torch.cuda.synchronize()
+        n_step = sum(a.elapsed_time(b) for a, b in nctx["ev"]) / args.steps
+        n_same = bool(torch.equal(nctx["out"], ctx["out"]))
+        more["decode_27b_noalloc"] = {
+            "workload": "the headline decode step through gqa_attn_decode_noalloc (no "
+                        "caller workspace)",
+            "value": round(step_bytes / (n_step / 1e3) / 1e9, 2), "unit": "GB/s",
+            "frac_of_hbm": round(step_bytes / (n_step / 1e3) / 1e9 / hbm_peak, 4),
+            "ms_per_step": round(n_step, 5), "same_bits_as_decode": n_same,
+            "launch": last_launch("decode_split_kernel")}
+        del nctx
+        torch.cuda.empty_cache()
         pff = S.prefill_27b(dtype=torch.float16)
         pff_ms = bench_prefill(pff, pf_steps, max(3, args.warmup), dev, e2e=False)[0]
         pff_avg = sum(pff_ms) / len(pff_ms)
@@ -722,15 +770,9 @@ def ours(args):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 Q/K/V, G ~ N(0,2)); no dataset",
-            "config": {
-                "workload": DECODE_WORKLOAD,
-                "bytes_per_step": step_bytes,
-                "kv_bytes_per_step": kv_bytes,
-                "split_plan": {"mode": "balanced shares (one per resident CTA)",
-                               "part_slots": BAL_PARTS},
-                "l2": "flushed before every timed step (256 MiB write, outside the events)",
-                "parallelism": f"replicas x{world} (no data-path collective)",
-            },
+            "config": decode_config(x),
+            "split_plan": {"mode": "balanced shares (one per resident CTA)",
+                           "part_slots": BAL_PARTS},
             "roofline": {
                 "kernel": "decode_split_kernel",
                 "bound": "hbm",
@@ -742,10 +784,7 @@ def ours(args):
                 "traffic": args.traffic if args.traffic is not None else
                 dram_traffic("decode_split_kernel", int(x.kv_lens.sum()) * x.k_cache.shape[1]),
                 "avg_launch_ms": round(split_avg, 5),
-                "launch": {"grid": 2 * torch.cuda.get_device_properties(dev).multi_processor_count,
-                           "block": 128, "dynamic_smem_bytes": 16 * 512 + 3 * 2 * 32 * 512,
-                           "packed_rows_per_cta": 16, "tile_keys": 32, "stages": 3,
-                           "part_slots": BAL_PARTS},
+                "launch": split_launch,
                 "timing": "events around gqa_attn_decode_split alone in the step's form "
                           "(balanced shares, 16 part slots), K steps right after the headline "
                           "steps, L2 flushed before each",
@@ -759,7 +798,7 @@ def ours(args):
                     "d2h_bytes_per_step": d2h,
                     "note": "gqa_attn_decode with pinned host Q/G/kv_lens in (one copy) and "
                             "out back (one copy); the KV cache is resident device state"},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": launches,
             "cpu_baseline": cpu,
             "prefill": {
                 "workload": "27B-shape prefill: B=1, Hq=24, Hkv=4, Lq=Lkv=8192 causal, "
@@ -769,9 +808,7 @@ def ours(args):
                 "flops_per_call": flops,
                 "avg_ms": round(pf_avg, 4),
                 "steps": pf_steps,
-                "launch": {"grid": -(-8192 // (128 // 6)) * 4, "block": 320,
-                           "rows_per_tile": 128 // 6, "heads_per_tile": 6, "tile_keys": 128,
-                           "tmem_columns": 512},
+                "launch": pf_launch,
                 "roofline": {"kernel": "attn_tc_kernel<prefill>", "bound": "tensor",
                              "achieved": round(pf_tflops, 2), "peak": bf16_peak,
                              "peak_source": f"{peak_src} bf16_tflops (burst)",
@@ -779,7 +816,11 @@ def ours(args):
                              "traffic": args.prefill_traffic if args.prefill_traffic is not None
                              else dram_traffic("attn_tc_kernel_prefill",
                                                (pf.q.numel() + pf.k.numel() + pf.v.numel() +
-                                                pf.g.numel()) * 2)},
+                                                pf.g.numel()) * 2),
+                             "traffic_note": "not measured on this launch: the DRAM bytes of "
+                                             "the 4,096-row capture, scaled by input bytes; "
+                                             "output writes still in L2 when that kernel "
+                                             "ended are not counted"},
                 "e2e": {"value": round(flops / (pf_e2e_avg / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                         "h2d_bytes_per_step": pf_h2d, "d2h_bytes_per_step": pf_d2h},
                 "device_status": pf_status,
@@ -828,10 +869,8 @@ def reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, G ~ N(0,2)); no dataset",
-        "config": {"workload": DECODE_WORKLOAD,
-                   "bytes_per_step": decode_bytes(x)[1],
-                   "sample": "each step a bounded sample of whole sequences (see cpu_baseline)",
-                   "parallelism": "rank 0 only (host cores)"},
+        "config": decode_config(x),
+        "sample": "each step a bounded sample of whole sequences (see cpu_baseline)",
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": _CORES,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -856,6 +895,8 @@ CASES = {
     # the prefill_4k inputs with an additive bf16 bias [4096, 4096] (N(0,2), seed 7,
     # 32 MB) broadcast over heads, causal: the general-mask kernel, staged mask rows
     "masked_4k": lambda: S.make_prefill(1, 24, 4, 4096, seed=2, outlier_frac=0.01),
+    # the 128-row prompt of the bench's tiny-prefill line (28 CTAs of one key tile)
+    "prefill_tiny": lambda: S.tiny_prefill(),
 }
 
 

@@ -21,7 +21,7 @@ HEAD_DIM = 256
 
 __all__ = ["prefill", "masked", "decode", "verify_tree", "kv_append", "kv_keep", "decode_plan", "decode_split", "lse_merge",
            "decode_workspace_size", "last_device_status", "set_wait_timeout_ns",
-           "selftest_wait_timeout", "GqaError",
+           "selftest_wait_timeout", "decode_noalloc", "launch_log", "GqaError",
            "load"]
 
 
@@ -187,6 +187,43 @@ def decode(q, k_cache, v_cache, g, kv_lens, cu_rows=None, max_rows=None, max_kv_
               workspace.numel() * workspace.element_size(), _stream())
     check(code, "gqa_attn_decode" + sfx)
     return (out, lse) if return_lse else out
+
+
+def decode_noalloc(q, k_cache, v_cache, g, kv_lens, cu_rows=None, max_rows=None,
+                   max_kv_len=None, out=None, return_lse=False):
+    """decode() through gqa_attn_decode_noalloc: the library's fixed 16 MiB area is the
+    workspace (bf16 only; calls whose workspace would not fit raise GQA_ERR_WORKSPACE).
+    Same kernels, plan and results as decode()."""
+    if q.dtype != torch.bfloat16:
+        raise TypeError("decode_noalloc takes bf16 inputs")
+    _need(q, q.dtype, 3, "q")
+    _need(k_cache, q.dtype, 4, "k_cache")
+    _need(v_cache, q.dtype, 4, "v_cache")
+    if g is not None:
+        _need(g, q.dtype, 3, "g")
+    T, Hq, B, Hkv, Lcap, max_rows, max_kv_len = _decode_sizes(q, k_cache, kv_lens, cu_rows,
+                                                               max_rows, max_kv_len)
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if return_lse else None
+    _need(out, q.dtype, 3, "out")
+    code = load().gqa_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(g),
+                                          _ptr(kv_lens), _ptr(cu_rows), _ptr(out), _ptr(lse), B,
+                                          T, Hq, Hkv, Lcap, max_rows, max_kv_len, _stream())
+    check(code, "gqa_attn_decode_noalloc")
+    return (out, lse) if return_lse else out
+
+
+def launch_log(n=64):
+    """The library's record of its last kernel launches (at most 64), newest first:
+    dicts of kernel, seq, grid, block, dynamic_smem, as the launches used them."""
+    from ._lib import LaunchInfo
+    buf = (LaunchInfo * n)()
+    got = load().gqa_launch_log(buf, n)
+    if got < 0:
+        check(-got, "gqa_launch_log")
+    return [{"kernel": r.kernel.decode(), "seq": int(r.seq), "grid": int(r.grid),
+             "block": int(r.block), "dynamic_smem": int(r.dynamic_smem)} for r in buf[:got]]
 
 
 def verify_tree(q, k_cache, v_cache, g, kv_lens, cu_rows, tree_mask, max_rows=None,

@@ -21,6 +21,15 @@ STATUS = {
     6: "GQA_ERR_DEVICE_RANGE",
 }
 
+
+
+class LaunchInfo(ctypes.Structure):
+    """gqa_launch_info of include/gqa_attn.h."""
+    _fields_ = [("kernel", ctypes.c_char * 64), ("seq", ctypes.c_ulonglong),
+                ("grid", ctypes.c_uint), ("block", ctypes.c_uint),
+                ("dynamic_smem", ctypes.c_uint)]
+
+
 # name -> (restype, argtypes); the exported symbols of include/gqa_attn.h
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -46,6 +55,7 @@ SIGNATURES = {
                                   _P, ctypes.c_size_t, _P]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      _P]),
+    "gqa_launch_log": (_I, [ctypes.POINTER(LaunchInfo), _I]),
     "gqa_attn_mask_check": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _I]),
     "gqa_attn_masked": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                              _I, _P]),

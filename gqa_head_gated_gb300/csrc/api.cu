@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "gqa_attn.h"
@@ -169,11 +170,6 @@ int decode_check_args(int B, int T, int Hq, int Hkv, int Lcap, int max_rows, int
                       bool has_cu_rows) {
   return check_decode_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, has_cu_rows);
 }
-void decode_plan_current_device(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int* S,
-                                int* C) {
-  plan_decode(B, Hq, Hkv, max_rows, max_kv_len, sm_count(), S, C);
-}
-size_t decode_workspace_bytes(int T, int Hq, int S) { return workspace_bytes_for(T, Hq, S); }
 bool make_launch_ctl(LaunchCtl* ctl) { return make_ctl(ctl); }
 
 namespace {
@@ -410,7 +406,34 @@ int gqa_attn_masked_impl(bool f16, const void* Q, const void* K, const void* V, 
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
+// The launch log: a ring of the last kLogSize launches, newest at (g_log_seq - 1).
+constexpr int kLogSize = 64;
+std::mutex g_log_mu;
+gqa_launch_info g_log[kLogSize];
+unsigned long long g_log_seq = 0;
+
 }  // namespace
+
+void note_launch(const char* kernel, long long grid, int block, size_t dynamic_smem) {
+  gqa_launch_info r{};
+  std::strncpy(r.kernel, kernel, sizeof(r.kernel) - 1);
+  r.grid = static_cast<unsigned int>(grid);
+  r.block = static_cast<unsigned int>(block);
+  r.dynamic_smem = static_cast<unsigned int>(dynamic_smem);
+  std::lock_guard<std::mutex> lock(g_log_mu);
+  r.seq = ++g_log_seq;
+  g_log[(r.seq - 1) % kLogSize] = r;
+}
+
+int decode_bf16_with_workspace(const void* Q, const void* Kcache, const void* Vcache,
+                               const void* G, const int* kv_lens, const int* cu_rows, void* out,
+                               float* lse_out, int B, int T, int Hq, int Hkv, int Lcap,
+                               int max_rows, int max_kv_len, void* workspace,
+                               size_t workspace_bytes, gqa_stream_t stream) {
+  return gqa_attn_decode_impl(false, Q, Kcache, Vcache, G, kv_lens, cu_rows, out, lse_out, B, T,
+                              Hq, Hkv, Lcap, max_rows, max_kv_len, workspace, workspace_bytes,
+                              stream);
+}
 
 }  // namespace gqa
 
@@ -553,6 +576,16 @@ int gqa_attn_masked_f16(const void* Q, const void* K, const void* V, const void*
   return gqa_attn_masked_impl(true, Q, K, V, G, mask, mask_kind, mask_shape, mask_strides, out,
                               lse_out, B, Hq, Hkv, Lq, Lkv, causal, kv_offset, head_chunking,
                               stream);
+}
+
+int gqa_launch_log(gqa_launch_info* out, int max_entries) {
+  if (max_entries < 0 || (out == nullptr && max_entries > 0)) return -GQA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_log_mu);
+  const unsigned long long have = g_log_seq < kLogSize ? g_log_seq : kLogSize;
+  const int n = static_cast<int>(have < static_cast<unsigned long long>(max_entries) ? have
+                                                                                     : max_entries);
+  for (int i = 0; i < n; ++i) out[i] = g_log[(g_log_seq - 1 - i) % kLogSize];
+  return n;
 }
 
 int gqa_last_device_status(gqa_stream_t stream) {

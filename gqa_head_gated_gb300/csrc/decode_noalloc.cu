@@ -6,9 +6,10 @@
 // can stall on device-wide synchronisation or fail under memory pressure in the
 // middle of a request), or a plug-in whose host application hands it only fixed
 // input and output buffers and owns all other device memory.
-// This entry point takes the same inputs and outputs as gqa_attn_decode but keeps
-// the split partial results in a fixed area of device memory that belongs to the
-// library, so the caller passes no workspace.
+// This entry point is gqa_attn_decode with a workspace that belongs to the library:
+// the same argument checks, plan, kernels and results, bit for bit, and the same
+// workspace rule (gqa_attn_decode_workspace_size() for the call must fit the area,
+// else GQA_ERR_WORKSPACE before any launch).
 //
 // The area is a file-scope __device__ array of kStaticScratchBytes (16 MiB).  Every
 // GPU that loads the library holds it until the process exits.  In host code the
@@ -16,8 +17,8 @@
 // with cudaGetSymbolAddress, once per device, with that device current, on the
 // first call made on that device; that first call should therefore come before
 // any stream capture.  All calls on a device share the one area and it keeps the
-// previous call's contents: nothing in it needs to start at zero (the split kernel
-// writes every partial row the merge reads), but two calls whose kernels overlap on
+// previous call's contents: nothing in it needs to start at zero (the split kernels
+// write every partial row the merge reads), but two calls whose kernels overlap on
 // the GPU (different streams, no ordering between them) race on it.
 #include <cuda_runtime.h>
 
@@ -64,29 +65,11 @@ int gqa_attn_decode_noalloc(const void* Q, const void* Kcache, const void* Vcach
   const int st = decode_check_args(B, T, Hq, Hkv, Lcap, max_rows, max_kv_len, cu_rows != nullptr);
   if (st != GQA_OK) return st;
   if (T == 0) return GQA_OK;
-  if (Q == nullptr || Kcache == nullptr || Vcache == nullptr || kv_lens == nullptr ||
-      out == nullptr)
-    return GQA_ERR_INVALID_ARG;
-  const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
-  if (!al(Q, 16) || !al(Kcache, 16) || !al(Vcache, 16) || !al(out, 16) ||
-      (G != nullptr && !al(G, 16)) || (lse_out != nullptr && !al(lse_out, 4)) ||
-      !al(kv_lens, 4) || (cu_rows != nullptr && !al(cu_rows, 4)))
-    return GQA_ERR_INVALID_ARG;
-  int S = 0, C = 0;
-  decode_plan_current_device(B, Hq, Hkv, max_rows, max_kv_len, &S, &C);
-  if (decode_workspace_bytes(T, Hq, S) > kStaticScratchBytes) return GQA_ERR_WORKSPACE;
   void* scratch = scratch_on_current_device();
-  LaunchCtl ctl;
-  if (scratch == nullptr || !make_launch_ctl(&ctl)) return GQA_ERR_CUDA;
-  float* O_parts = static_cast<float*>(scratch);
-  float* lse_parts = O_parts + size_t(S) * size_t(T) * Hq * 256;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  DecodeSplitArgs a{Q, Kcache, Vcache, kv_lens, cu_rows, O_parts, lse_parts, B, T, Hq, Hkv,
-                    Lcap, max_rows, max_kv_len, S, C};
-  if (launch_decode_split(a, ctl, s) != cudaSuccess) return GQA_ERR_CUDA;
-  MergeArgs m{O_parts, lse_parts, S, T * Hq, G, out, lse_out};
-  m.after_split = true;
-  return launch_lse_merge(m, ctl, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  if (scratch == nullptr) return GQA_ERR_CUDA;
+  return decode_bf16_with_workspace(Q, Kcache, Vcache, G, kv_lens, cu_rows, out, lse_out, B, T,
+                                    Hq, Hkv, Lcap, max_rows, max_kv_len, scratch,
+                                    kStaticScratchBytes, stream);
 }
 
 }  // extern "C"

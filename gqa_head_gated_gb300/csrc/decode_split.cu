@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <type_traits>
 
 #include "internal.h"
@@ -624,7 +625,14 @@ cudaError_t launch_t(const Params& p, cudaStream_t stream, long long grid) {
     grid = (long long)(per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
   }
   decode_split_kernel<WR, WK, kF16><<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    char name[64];
+    std::snprintf(name, sizeof(name), "decode_split_kernel<%d,%d,%s>%s", WR, WK,
+                  kF16 ? "fp16" : "bf16", p.balanced ? " balanced" : "");
+    note_launch(name, grid, kThreads, smem);
+  }
+  return e;
 }
 
 }  // namespace

@@ -87,12 +87,20 @@ struct MergeArgs {
 
 cudaError_t launch_lse_merge(const MergeArgs& a, const LaunchCtl& ctl, cudaStream_t stream);
 
-// Host-side pieces of gqa_attn_decode shared with the no-allocation entry point.
+// Notes a kernel launch in the library's launch log (gqa_launch_log); `kernel` is
+// copied (at most 63 characters).  Call it after the launch call succeeded.
+void note_launch(const char* kernel, long long grid, int block, size_t dynamic_smem);
+
+// gqa_attn_decode's host side, shared with the no-allocation entry point: its argument
+// checks, and the whole call (checks, plan, kernels) with a given workspace.
 int decode_check_args(int B, int T, int Hq, int Hkv, int Lcap, int max_rows, int max_kv_len,
                       bool has_cu_rows);
-void decode_plan_current_device(int B, int Hq, int Hkv, int max_rows, int max_kv_len, int* S,
-                                int* C);
-size_t decode_workspace_bytes(int T, int Hq, int S);
+// The launch control block (status word, wait bound) for the current device.
 bool make_launch_ctl(LaunchCtl* ctl);
+int decode_bf16_with_workspace(const void* Q, const void* Kcache, const void* Vcache,
+                               const void* G, const int* kv_lens, const int* cu_rows, void* out,
+                               float* lse_out, int B, int T, int Hq, int Hkv, int Lcap,
+                               int max_rows, int max_kv_len, void* workspace,
+                               size_t workspace_bytes, gqa_stream_t stream);
 
 }  // namespace gqa

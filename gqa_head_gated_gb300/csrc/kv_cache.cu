@@ -139,7 +139,9 @@ int gqa_kv_append(const void* Knew, const void* Vnew, const int* cu_rows, const 
   kv_append_kernel<<<dim3(unsigned(grid)), kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(Knew), static_cast<const uint4*>(Vnew), cu_rows, kv_lens,
       static_cast<uint4*>(Kcache), static_cast<uint4*>(Vcache), B, T, Hkv, Lcap, ctl);
-  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  note_launch("kv_append_kernel", grid, kWarps * 32, 0);
+  return GQA_OK;
 }
 
 int gqa_kv_keep(void* Kcache, void* Vcache, const int* kv_lens, const int* cu_rows,
@@ -160,7 +162,9 @@ int gqa_kv_keep(void* Kcache, void* Vcache, const int* kv_lens, const int* cu_ro
   kv_keep_kernel<<<dim3(unsigned(grid)), kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<uint4*>(Kcache), static_cast<uint4*>(Vcache), kv_lens, cu_rows, keep_idx,
       cu_keep, kv_lens_out, B, Hkv, Lcap, ctl);
-  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  note_launch("kv_keep_kernel", grid, kWarps * 32, 0);
+  return GQA_OK;
 }
 
 }  // extern "C"

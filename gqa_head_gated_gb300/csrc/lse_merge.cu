@@ -127,7 +127,10 @@ cudaError_t launch_merge_t(const MergeArgs& a, long long grid, cudaStream_t stre
     lse_merge_kernel<kF16><<<dim3(unsigned(grid)), dim3(kWarps * 32), 0, stream>>>(
         a.O_parts, a.lse_parts, a.S, a.N, static_cast<const uint16_t*>(a.G),
         static_cast<uint16_t*>(a.out), a.lse_out, 0);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+      note_launch(kF16 ? "lse_merge_kernel<fp16>" : "lse_merge_kernel<bf16>", grid, kWarps * 32, 0);
+    return e;
   }
   // Right after the library's split kernel: programmatic dependent launch, so the
   // merge may be scheduled while that kernel drains; it waits for it in
@@ -142,9 +145,14 @@ cudaError_t launch_merge_t(const MergeArgs& a, long long grid, cudaStream_t stre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<kF16>, a.O_parts, a.lse_parts, a.S, a.N,
-                            static_cast<const uint16_t*>(a.G), static_cast<uint16_t*>(a.out),
-                            a.lse_out, 1);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, lse_merge_kernel<kF16>, a.O_parts, a.lse_parts, a.S, a.N,
+                         static_cast<const uint16_t*>(a.G), static_cast<uint16_t*>(a.out),
+                         a.lse_out, 1);
+  if (e == cudaSuccess)
+    note_launch(kF16 ? "lse_merge_kernel<fp16> dependent" : "lse_merge_kernel<bf16> dependent",
+                grid, kWarps * 32, 0);
+  return e;
 }
 
 }  // namespace

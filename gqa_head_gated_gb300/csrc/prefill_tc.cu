@@ -1236,7 +1236,13 @@ cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   if (e != cudaSuccess) return e;
   attn_tc_kernel<kSplit, kF16, kMask><<<dim3(unsigned(grid)), dim3(cta_threads<kMask>()), smem,
                                         stream>>>(tq, tk, tv, tg, to, p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess)
+    note_launch(kSplit  ? (kF16 ? "attn_tc_kernel<split,fp16>" : "attn_tc_kernel<split,bf16>")
+                : kMask ? (kF16 ? "attn_tc_kernel<masked,fp16>" : "attn_tc_kernel<masked,bf16>")
+                        : (kF16 ? "attn_tc_kernel<prefill,fp16>" : "attn_tc_kernel<prefill,bf16>"),
+                grid, cta_threads<kMask>(), smem);
+  return e;
 }
 
 }  // namespace

@@ -41,5 +41,7 @@ extern "C" int gqa_selftest_wait_timeout(unsigned long long* elapsed_ns, gqa_str
   LaunchCtl ctl;
   if (!make_launch_ctl(&ctl)) return GQA_ERR_CUDA;
   wait_timeout_probe<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ctl, elapsed_ns);
-  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  note_launch("wait_timeout_probe", 1, 32, 0);
+  return GQA_OK;
 }

@@ -209,11 +209,12 @@ int attn_lse_merge(const float* O_parts, const float* lse_parts, int S, int N,
  * stall on device-wide synchronisation or fail under memory pressure mid-request),
  * plug-ins whose host application hands them only fixed input and output buffers.
  * The paper has
- * no counterpart: this is a library convenience.  Same inputs, outputs, rules and
- * results as gqa_attn_decode, but the split partial results live in a fixed
- * 16 MiB area of device memory owned by the library (a file-scope __device__ array,
- * held by every GPU that loads the library until the process exits), so the caller
- * passes no workspace; the call itself allocates nothing.
+ * no counterpart: this is a library convenience.  It is gqa_attn_decode with a
+ * workspace owned by the library: the same inputs, outputs, argument checks, plan,
+ * kernels and results (bit for bit), but the split partial results live in a fixed
+ * 16 MiB area of device memory (a file-scope __device__ array, held by every GPU
+ * that loads the library until the process exits), so the caller passes no
+ * workspace; the call itself allocates nothing.
  * Limit: gqa_attn_decode_workspace_size() for the same sizes must not exceed
  * 16 MiB (16,777,216 bytes); larger calls return GQA_ERR_WORKSPACE and launch
  * nothing.
@@ -226,6 +227,26 @@ int gqa_attn_decode_noalloc(const void* Q, const void* Kcache, const void* Vcach
                             const void* G, const int* kv_lens, const int* cu_rows, void* out,
                             float* lse_out, int B, int T, int Hq, int Hkv, int Lcap,
                             int max_rows, int max_kv_len, gqa_stream_t stream);
+
+/*
+ * Launch log: the library notes, on the host, every kernel launch it makes - the
+ * kernel and its instance, and the grid, block and dynamic shared memory the launch
+ * used - in a ring holding the last 64 launches of the process.  gqa_launch_log
+ * copies up to max_entries of them into `out` (host memory owned by the caller),
+ * newest first, and returns how many it copied (0 before any launch).  A launch
+ * the CUDA runtime refused is not logged.  Returns GQA_ERR_INVALID_ARG (as a
+ * negative number, -1) for max_entries < 0, or for out == NULL with
+ * max_entries > 0.  Thread-safe; makes no CUDA call.
+ */
+typedef struct gqa_launch_info {
+  char kernel[64];              /* kernel and instance, NUL-terminated */
+  unsigned long long seq;       /* 1 for the process's first launch, then 2, 3, ... */
+  unsigned int grid;            /* CTAs (the grids are one-dimensional) */
+  unsigned int block;           /* threads per CTA */
+  unsigned int dynamic_smem;    /* bytes of dynamic shared memory per CTA */
+} gqa_launch_info;
+
+int gqa_launch_log(gqa_launch_info* out, int max_entries);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word that the

@@ -7,6 +7,7 @@ import re
 
 import pytest
 
+import gqa_head_gated_gb300 as G
 from gqa_head_gated_gb300 import _lib
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -40,6 +41,16 @@ def test_exports_every_declared_function(lib):
     for n in sorted(names):
         assert hasattr(lib, n), f"libgqa_attn.so does not export {n}"
     assert set(_lib.SIGNATURES) == names
+
+
+def test_launch_log_without_launches(lib):
+    """No kernel has run in this (GPU-less) process: the log is empty, and bad
+    arguments are refused with -GQA_ERR_INVALID_ARG."""
+    assert G.launch_log() == []
+    assert lib.gqa_launch_log(None, 0) == 0
+    assert lib.gqa_launch_log(None, 4) == -1
+    buf = (_lib.LaunchInfo * 2)()
+    assert lib.gqa_launch_log(buf, -1) == -1
 
 
 def test_status_strings(lib):

@@ -74,6 +74,11 @@ PREFILL = {
     "gqa8": ((1, 16, 2, 257, 400, 143),
              [("v_inf", 0, 150, 1), ("v_ninf", 0, 151, 2), ("v_nan", 1, 399, 3),
               ("k_nan", 1, 300, 4)]),
+    # GQA 1 at offset 64: the first row tile's diagonal spans keys 65..191 and its
+    # second key tile runs to key 255, so 180 planted keys are hidden from some of its
+    # rows (more than 128 in one CTA)
+    "gqa1_many": ((1, 4, 4, 256, 320, 64),
+                  [("v_nan" if k % 3 else "v_inf", 0, k, k % 256) for k in range(65, 245)]),
 }
 
 
