@@ -279,7 +279,7 @@ def last_launch(prefix):
     name starts with `prefix`: grid, block and dynamic shared memory as launched."""
     import gqa_head_gated_gb300 as G
     for r in G.launch_log():
-        if r["kernel"].startswith(prefix):
+        if r["kernel"].startswith(prefix):   # a string or a tuple of prefixes
             return {"kernel": r["kernel"], "grid": r["grid"], "block": r["block"],
                     "dynamic_smem_bytes": r["dynamic_smem"], "source": "gqa_launch_log"}
     return None
@@ -558,7 +558,7 @@ def ours(args):
     pf_steps = max(3, min(args.steps, 10))
     pf_ms, pf_status, pf_e2e, pf_h2d, pf_d2h, pf_clk = bench_prefill(pf, pf_steps,
                                                                      max(3, args.warmup), dev)
-    pf_launch = last_launch("attn_tc_kernel<prefill")
+    pf_launch = last_launch(("attn_tc_kernel<prefill", "attn_pair_kernel<prefill"))
     pf_avg = sum(pf_ms) / len(pf_ms)
     pf_tflops = flops / (pf_avg / 1e3) / 1e12
     bf16_peak = float(peaks["bf16_tflops"])
@@ -809,12 +809,14 @@ def ours(args):
                 "avg_ms": round(pf_avg, 4),
                 "steps": pf_steps,
                 "launch": pf_launch,
-                "roofline": {"kernel": "attn_tc_kernel<prefill>", "bound": "tensor",
+                "roofline": {"kernel": pf_launch["kernel"] if pf_launch else None, "bound": "tensor",
                              "achieved": round(pf_tflops, 2), "peak": bf16_peak,
                              "peak_source": f"{peak_src} bf16_tflops (burst)",
                              "unit": "TFLOP/s", "frac": round(pf_tflops / bf16_peak, 4),
                              "traffic": args.prefill_traffic if args.prefill_traffic is not None
-                             else dram_traffic("attn_tc_kernel_prefill",
+                             else dram_traffic("attn_pair_kernel_prefill"
+                                               if pf_launch and pf_launch["kernel"].startswith("attn_pair")
+                                               else "attn_tc_kernel_prefill",
                                                (pf.q.numel() + pf.k.numel() + pf.v.numel() +
                                                 pf.g.numel()) * 2),
                              "traffic_note": "not measured on this launch: the DRAM bytes of "

@@ -19,7 +19,7 @@ from ._lib import GqaError, check, load  # noqa: F401
 
 HEAD_DIM = 256
 
-__all__ = ["prefill", "masked", "decode", "verify_tree", "kv_append", "kv_keep", "decode_plan", "decode_split", "lse_merge",
+__all__ = ["prefill", "prefill_pair", "masked", "decode", "verify_tree", "kv_append", "kv_keep", "decode_plan", "decode_split", "lse_merge",
            "decode_workspace_size", "last_device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "decode_noalloc", "launch_log", "GqaError",
            "load"]
@@ -77,6 +77,28 @@ def prefill(q, k, v, g=None, kv_offset=0, out=None, return_lse=False):
     code = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq, Lkv,
               int(kv_offset), _stream())
     check(code, "gqa_attn_prefill" + sfx)
+    return (out, lse) if return_lse else out
+
+
+def prefill_pair(q, k, v, g=None, kv_offset=0, out=None, return_lse=False):
+    """prefill() through gqa_attn_prefill_pair (CTA pairs sharing each K/V tile);
+    bf16 only."""
+    if q.dtype != torch.bfloat16:
+        raise TypeError("prefill_pair takes bf16 inputs")
+    _need(q, q.dtype, 4, "q")
+    _need(k, q.dtype, 4, "k")
+    _need(v, q.dtype, 4, "v")
+    if g is not None:
+        _need(g, q.dtype, 4, "g")
+    B, Hq, Lq, _ = q.shape
+    Hkv, Lkv = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device) if return_lse else None
+    _need(out, q.dtype, 4, "out")
+    code = load().gqa_attn_prefill_pair(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(lse),
+                                        B, Hq, Hkv, Lq, Lkv, int(kv_offset), _stream())
+    check(code, "gqa_attn_prefill_pair")
     return (out, lse) if return_lse else out
 
 

@@ -38,6 +38,7 @@ SIGNATURES = {
     "gqa_status_string": (ctypes.c_char_p, [_I]),
     "gqa_version": (ctypes.c_char_p, []),
     "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "gqa_attn_prefill_pair": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gqa_attn_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                              ctypes.c_size_t, _P]),

@@ -177,7 +177,7 @@ namespace {
 // Entry points for both element types; the extern "C" functions below pick one.
 int gqa_attn_prefill_impl(bool f16, const void* Q, const void* K, const void* V, const void* G,
                           void* out, float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv,
-                          int kv_offset, gqa_stream_t stream) {
+                          int kv_offset, gqa_stream_t stream, bool pair = false) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq < 0 || Lkv < 1 || kv_offset < 0 ||
       (long long)kv_offset + Lq > Lkv)
     return GQA_ERR_INVALID_ARG;
@@ -189,14 +189,17 @@ int gqa_attn_prefill_impl(bool f16, const void* Q, const void* K, const void* V,
   if (Hq / Hkv > 128) return GQA_ERR_UNSUPPORTED;
   if ((long long)Hq * Lq >= (1LL << 31) || (long long)B * Hkv >= (1LL << 31))
     return GQA_ERR_UNSUPPORTED;
-  const long long grid = (long long)ceil_div(Lq, prefill_rows_per_tile(Hq / Hkv)) * B * Hkv;
+  // (the CTA-pair form rounds the row tiles up to pairs)
+  const long long grid = (long long)(ceil_div(Lq, prefill_rows_per_tile(Hq / Hkv)) + 1) * B * Hkv;
   if (grid >= (1LL << 31)) return GQA_ERR_UNSUPPORTED;
   LaunchCtl ctl;
   if (!make_ctl(&ctl)) return GQA_ERR_CUDA;
   PrefillArgs a{Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset};
   a.f16 = f16;
   bool encode_failed = false;
-  const cudaError_t e = launch_prefill(a, ctl, static_cast<cudaStream_t>(stream), &encode_failed);
+  const cudaError_t e =
+      pair ? launch_prefill_pair(a, ctl, static_cast<cudaStream_t>(stream), &encode_failed)
+           : launch_prefill(a, ctl, static_cast<cudaStream_t>(stream), &encode_failed);
   if (encode_failed) return GQA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -471,6 +474,12 @@ int gqa_attn_prefill_f16(const void* Q, const void* K, const void* V, const void
                          gqa_stream_t stream) {
   return gqa_attn_prefill_impl(true, Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset,
                                stream);
+}
+int gqa_attn_prefill_pair(const void* Q, const void* K, const void* V, const void* G, void* out,
+                          float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv, int kv_offset,
+                          gqa_stream_t stream) {
+  return gqa_attn_prefill_impl(false, Q, K, V, G, out, lse_out, B, Hq, Hkv, Lq, Lkv, kv_offset,
+                               stream, true);
 }
 
 int gqa_attn_decode_plan(int B, int T, int Hq, int Hkv, int max_rows, int max_kv_len,

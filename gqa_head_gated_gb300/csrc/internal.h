@@ -36,6 +36,11 @@ inline int prefill_rows_per_tile(int gqa) { return 128 / gqa; }
 // Sets *encode_failed when a TMA descriptor could not be built.
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStream_t stream,
                            bool* encode_failed);
+// The plain (causal, unmasked) prefill on CTA pairs (gqa_attn_prefill_pair; and
+// gqa_attn_prefill when the last row sees at least kPairMinKeys keys).
+constexpr int kPairMinKeys = 2048;
+cudaError_t launch_prefill_pair(const PrefillArgs& a, const LaunchCtl& ctl, cudaStream_t stream,
+                                bool* encode_failed);
 
 struct DecodeSplitArgs {
   const void* Q;

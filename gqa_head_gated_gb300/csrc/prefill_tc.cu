@@ -69,42 +69,26 @@
 
 #include "internal.h"
 #include "ptx_sm100.cuh"
+#include "tc_common.cuh"
 
 namespace gqa {
 namespace {
 
-constexpr int kM = 128;                       // packed rows per tile
-constexpr int kN = 128;                       // keys per K/V tile
 constexpr int kKS = 1;                        // K ring slots (whole tiles)
 constexpr int kVS = 1;                        // V ring slots
 constexpr int kSlots = kKS + kVS;
-constexpr int kQChunk = 128 * 128;            // Q: 128 rows x 64 bf16 per column block
-constexpr int kQBytes = 4 * kQChunk;
-constexpr int kChunkBytes = kN * 128;         // K/V: kN rows x 64 bf16 per column block
-constexpr int kTileBytes = 4 * kChunkBytes;   // kN keys x 256 bf16
-constexpr int kHalf = kN / 2;                 // keys per softmax thread per tile
-static_assert(kN == 64 || kN == 128, "key tile of 64 or 128");
 static_assert(kSlots * kTileBytes >= kQBytes, "the output tile is staged in the K/V ring");
 constexpr int kThreads = 320;
-constexpr uint32_t kTmemCols = 512;
 // Cleaning pass: keys whose V rows held a NaN / Inf element among the candidate keys
 // (see cand_lo in the kernel); at most kMaxHits per CTA are handled exactly (rows past
 // that are left as they are).  A causal prompt tile's candidates (its diagonal and the
 // rest of its last key tile) and a verify tile's are fewer than 256; a general mask
 // makes every key a candidate.
 constexpr int kMaxHits = 256;
-static_assert(kN == 128, "the cleaning pass splits a tile's keys over two 64-key halves");
 // General masks with one mask head for all query heads: the tile's mask rows (R query
 // rows x kN keys, each row padded by 16 bytes so that reads of different rows fall on
 // different banks) are staged in two slots behind the Smem block.
 constexpr int kMaskSlotBytes = 11264;
-constexpr uint32_t kTmO = 0;
-constexpr uint32_t kTmS = 256;                // S buffer b at kTmS + kN*b
-// Lazy-rescale threshold in log2 units: P <= 2^threshold must fit the element type
-// (bf16: 2^32, fp16: 2^8, below its 65504 maximum).
-template <bool kF16>
-__device__ __forceinline__ float rescale_threshold() { return kF16 ? 8.0f : 32.0f; }
-
 template <bool kF16>
 constexpr uint32_t idesc_s() { return ptx::idesc_f32acc(kM, kN, 0, 0, kF16 ? 0u : 1u); }   // Q, K K-major
 template <bool kF16>
@@ -163,66 +147,9 @@ struct Params {
   LaunchCtl ctl;
 };
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
-
-// Position in a ring of tile slots [base, base + n): slot, phase bit, tiles so far.
-struct Ring {
-  int slot;
-  uint32_t phase;
-  int count;
-  int n;
-  int base;
-  __device__ __forceinline__ int at() const { return base + slot; }
-  __device__ __forceinline__ void advance() {
-    ++count;
-    if (++slot == n) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
 __device__ __forceinline__ void fail(Smem& sm, const Params& p) {
   sm.abort = 1;
   record_status(p.ctl.status, GQA_ERR_TIMEOUT);
-}
-
-// Item `it` of the load / consume sequence K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}.
-__device__ __forceinline__ void item_kind(int it, int n, bool& is_v, int& j) {
-  if (it == 0) {
-    is_v = false; j = 0;
-  } else if (it == 2 * n - 1) {
-    is_v = true; j = n - 1;
-  } else {
-    const int m = (it - 1) >> 1;
-    is_v = ((it - 1) & 1) != 0;
-    j = is_v ? m : m + 1;
-  }
-}
-
-// Bias of one mask element in natural-log units: a bool mask gives 0 (attend) or
-// -inf (excluded); an additive mask gives its value.
-__device__ __forceinline__ float mask_bias(uint8_t v) { return v ? 0.f : -INFINITY; }
-__device__ __forceinline__ float mask_bias(float v) { return v; }
-__device__ __forceinline__ float mask_bias(uint16_t v, std::integral_constant<int, 3>) {
-  return __uint_as_float(uint32_t(v) << 16);                       // bf16
-}
-__device__ __forceinline__ float mask_bias(uint16_t v, std::integral_constant<int, 4>) {
-  return __half2float(__ushort_as_half(v));                         // fp16
-}
-
-template <int kKind, typename E>
-__device__ __forceinline__ float mask_elem(E v) {
-  if constexpr (kKind == 3 || kKind == 4)
-    return mask_bias(v, std::integral_constant<int, kKind>{});
-  else
-    return mask_bias(v);
 }
 
 // Applies the mask to one row's raw scores s[0..n) (keys key0 .. key0+n-1, keys at
@@ -280,124 +207,6 @@ static_assert(sizeof(Smem) + 1024 + 16 + 2 * kMaskSlotBytes <= 227 * 1024,
 template <bool kMask>
 constexpr int cta_threads() { return kMask ? kThreads + 32 : kThreads; }
 
-
-// ---------------------------------------------------------------- non-finite V values
-// Out-of-line helpers of the cleaning pass (a NaN / Inf V element at a key that some
-// rows of a tile see and others do not; see the kernel).
-
-// Bits c of the result: key rows c of a landed V tile found holding a NaN / Inf
-// element (which is set to +0 in shared memory), among the rows selected by `rows`;
-// their keys (tile_key0 + c) are appended to the hit list from index `n`, up to
-// kMaxHits (rows past that are left as they are).  One warp.
-struct HitRows {
-  uint32_t w[kN / 32];
-  int n;          // hit-list length afterwards
-  bool wrote;     // this lane wrote shared memory
-};
-template <bool kF16>
-__device__ __noinline__ HitRows clean_rows(Smem& sm, uint8_t* vt, uint4 rows, int tile_key0,
-                                           int n) {
-  const int lane = threadIdx.x & 31;
-  const int blk = lane >> 3, ch = lane & 7;   // this lane's 16-byte chunk of a key row
-  HitRows h{{0u, 0u, 0u, 0u}, n, false};
-  const uint32_t rw[4] = {rows.x, rows.y, rows.z, rows.w};
-  for (int w = 0; w < kN / 32; ++w) {
-    uint32_t bits = rw[w];
-    while (bits != 0u) {
-      const int c = w * 32 + __ffs(bits) - 1;
-      bits &= bits - 1u;
-      uint4* const a =
-          reinterpret_cast<uint4*>(vt + blk * kChunkBytes + c * 128 + ((ch ^ (c & 7)) << 4));
-      uint4 u = *a;
-      const bool nf = clear_nonfinite<kF16>(u);
-      if (__ballot_sync(0xffffffffu, nf) != 0u && h.n < kMaxHits) {
-        if (nf) {
-          *a = u;
-          h.wrote = true;
-        }
-        h.w[w] |= 1u << (c & 31);
-        if (lane == 0) sm.hit_key[h.n] = tile_key0 + c;
-        ++h.n;
-      }
-    }
-  }
-  return h;
-}
-
-// Reads this thread's 64 probabilities of a cleaned tile back from P in tensor memory
-// and records, for the hit keys among them (bits of w0, w1; hit-list indices from
-// idx), whether the probability the P.V product used was 0.  Whole warp.
-__device__ __noinline__ void record_zero_probs(Smem& sm, uint32_t p_taddr, uint32_t w0,
-                                               uint32_t w1, int idx, int row) {
-  uint32_t pw[32];
-  ptx::tc_fence_after();
-  ptx::tmem_ld32_wait(p_taddr, pw);
-#pragma unroll 1
-  for (int c = 0; c < kHalf; ++c) {
-    if (((c < 32 ? w0 >> c : w1 >> (c - 32)) & 1u) != 0u) {
-      if (((pw[c >> 1] >> ((c & 1) * 16)) & 0xFFFFu) == 0u)
-        atomicOr(&sm.pz[row][idx >> 5], 1u << (idx & 31));
-      ++idx;
-    }
-  }
-}
-
-// Epilogue of a CTA with hits: adds p * V of the original NaN / Inf elements of every
-// hit key this row sees to its O row in tensor memory (o_taddr: the thread's 128
-// columns).  The sum is then a NaN or an infinity, so the scale of p does not matter;
-// a probability of 0 gives NaN, as float64 arithmetic would.  Whole warp; `act` says
-// whether this lane's row takes part.  vrow0: V row 0 of the KV head, at the thread's
-// first column.
-template <bool kF16, bool kMask>
-__device__ __noinline__ void add_hit_terms(const Smem& sm, uint32_t o_taddr, int row, int n_hits,
-                                           bool act, const uint16_t* vrow0, int lim, int tbase,
-                                           unsigned long long tmask, const void* mask,
-                                           int mask_kind, long long mrow, long long ms_j) {
-  ptx::tc_fence_after();
-#pragma unroll 1
-  for (int cc = 0; cc < 4; ++cc) {
-    uint32_t o[32];
-    ptx::tmem_ld32_wait(o_taddr + 32u * cc, o);
-    for (int i = 0; act && i < n_hits; ++i) {
-      const int key = sm.hit_key[i];
-      if (key >= lim) continue;
-      if (key >= tbase && key - tbase < 64 && !((tmask >> (key - tbase)) & 1ull)) continue;
-      if constexpr (kMask) {
-        const long long at = mrow + (long long)key * ms_j;
-        float a = 0.f;
-        switch (mask_kind) {
-          case 1: a = mask_elem<1>(static_cast<const uint8_t*>(mask)[at]); break;
-          case 2: a = mask_elem<2>(static_cast<const float*>(mask)[at]); break;
-          case 3: a = mask_elem<3>(static_cast<const uint16_t*>(mask)[at]); break;
-          case 4: a = mask_elem<4>(static_cast<const uint16_t*>(mask)[at]); break;
-          default: break;
-        }
-        if (a == -INFINITY) continue;
-      }
-      const float keep = ((sm.pz[row][i >> 5] >> (i & 31)) & 1u) ? 0.f : 1.f;
-      const uint4* const v = reinterpret_cast<const uint4*>(vrow0 + (long long)key * kHeadDim + cc * 32);
-#pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint4 u = __ldg(v + q4);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll 1
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t x = (w[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu;
-          if (elem_nonfinite<kF16>(x))
-            o[q4 * 8 + e] =
-                __float_as_uint(__uint_as_float(o[q4 * 8 + e]) + keep * elem_to_float<kF16>(x));
-        }
-      }
-    }
-    ptx::tmem_st32_wait(o_taddr + 32u * cc, o);
-  }
-}
-
-
-// Ring position after `count` uses of a ring of n slots that starts at slot `base`.
-__device__ __forceinline__ Ring ring_after(int count, int n, int base) {
-  return Ring{count % n, uint32_t(count / n) & 1u, count, n, base};
-}
 
 template <bool kSplit, bool kF16, bool kMask>
 __global__ void __launch_bounds__(cta_threads<kMask>(), 1)
@@ -551,6 +360,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             ptx::tma_load_3d(sm.q + dc * kQChunk, &tmQ, &sm.q_full, dc * 64, g * p.gqa, t0 + r0);
         }
       }
+      // Lane 0: the copy of K_j or V_j into its ring slot, once the slot's previous
+      // use is done.
+      auto issue_copy = [&](const Ring& r, bool is_v, int j) -> bool {
+        const int slot = r.at();
+        if (r.count >= r.n &&
+            !ptx::mbar_wait(&sm.kv_empty[slot], r.phase ^ 1u, tmo, &sm.abort))
+          return false;
+        ptx::mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
+        const CUtensorMap* tm = is_v ? &tmV : &tmK;
+        for (int dc = 0; dc < 4; ++dc)
+          ptx::tma_load_3d(sm.kv[slot] + dc * kChunkBytes, tm, &sm.kv_full[slot], dc * 64,
+                           (j0 + j) * kN, bg);
+        return true;
+      };
       if constexpr (!kClean) {
         if (lane == 0) {
           const int total = 2 * n_tiles;
@@ -559,17 +382,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             int j;
             item_kind(it, n_tiles, is_v, j);
             Ring& r = is_v ? rv : rk;
-            const int slot = r.at();
-            if (r.count >= r.n &&
-                !ptx::mbar_wait(&sm.kv_empty[slot], r.phase ^ 1u, tmo, &sm.abort)) {
+            if (!issue_copy(r, is_v, j)) {
               fail(sm, p);
               break;
             }
-            ptx::mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
-            const CUtensorMap* tm = is_v ? &tmV : &tmK;
-            for (int dc = 0; dc < 4; ++dc)
-              ptx::tma_load_3d(sm.kv[slot] + dc * kChunkBytes, tm, &sm.kv_full[slot], dc * 64,
-                               (j0 + j) * kN, bg);
             r.advance();
           }
         }
@@ -591,18 +407,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           Ring& r = is_v ? rv : rk;
           const int slot = r.at();
           int go = 1;
-          if (lane == 0) {
-            if (r.count >= r.n &&
-                !ptx::mbar_wait(&sm.kv_empty[slot], r.phase ^ 1u, tmo, &sm.abort)) {
-              go = 0;
-            } else {
-              ptx::mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
-              const CUtensorMap* tm = is_v ? &tmV : &tmK;
-              for (int dc = 0; dc < 4; ++dc)
-                ptx::tma_load_3d(sm.kv[slot] + dc * kChunkBytes, tm, &sm.kv_full[slot], dc * 64,
-                                 (j0 + j) * kN, bg);
-            }
-          }
+          if (lane == 0) go = issue_copy(r, is_v, j) ? 1 : 0;
           if (__shfl_sync(0xffffffffu, go, 0) == 0) {
             if (lane == 0) fail(sm, p);
             break;
@@ -1195,36 +1000,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-bool encode_16b(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank,
-                const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
-                bool f16) {
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base),
-                  dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <bool kSplit, bool kF16, bool kMask = false>
 cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const CUtensorMap& tg, const CUtensorMap& to, const Params& p,
@@ -1249,6 +1024,12 @@ cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtl& ctl, cudaStream_t stream,
                            bool* encode_failed) {
+  // Long prompts run on CTA pairs, which copy and read half of every K/V tile per SM:
+  // on GB300 that matches this kernel at 4K-8K keys and is faster when the rows see
+  // many more keys than the row tiles hold (L2 traffic halves), while a short prompt
+  // pays the pair's cluster set-up.
+  if (!a.masked && a.kv_offset + a.Lq >= kPairMinKeys)
+    return launch_prefill_pair(a, ctl, stream, encode_failed);
   *encode_failed = false;
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) {

@@ -96,11 +96,25 @@ const char* gqa_version(void);
  * kv_offset + Lq - 1 are never read (they may hold anything, NaN included).
  * Requires B, Hq, Hkv >= 1, Hq % Hkv == 0, Hq/Hkv <= 128, Lq >= 0,
  * kv_offset >= 0, kv_offset + Lq <= Lkv, Lkv < 2^31.
- * Runs on tcgen05 tensor cores (TMEM accumulators, TMA-staged tiles).
+ * Runs on tcgen05 tensor cores (TMEM accumulators, TMA-staged tiles); a prompt
+ * whose last row sees 2048 keys or more (kv_offset + Lq >= 2048) runs on CTA pairs
+ * (see gqa_attn_prefill_pair), a shorter one on single CTAs.
  */
 int gqa_attn_prefill(const void* Q, const void* K, const void* V, const void* G,
                      void* out, float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv,
                      int kv_offset, gqa_stream_t stream);
+
+/*
+ * gqa_attn_prefill computed by CTA pairs whatever the prompt length: two CTAs of a
+ * cluster take two row tiles of a KV group and share each 128-key K/V tile (each
+ * copies half of it; the products, tcgen05 .cta_group::2 with M = 256, read both
+ * halves).  Same arguments, rules, errors and results (within the parity bar; the
+ * single-CTA form may differ in the last bit of an output) as gqa_attn_prefill,
+ * which picks this form for long prompts by itself.
+ */
+int gqa_attn_prefill_pair(const void* Q, const void* K, const void* V, const void* G,
+                          void* out, float* lse_out, int B, int Hq, int Hkv, int Lq, int Lkv,
+                          int kv_offset, gqa_stream_t stream);
 
 /*
  * Decode (one row per sequence) and chain verify (r_b rows per sequence, causal

@@ -22,6 +22,20 @@ def test_prefill_launch_is_logged():
     assert rec["dynamic_smem"] > 200 * 1024
 
 
+def test_long_prefill_runs_on_cta_pairs():
+    """A prompt whose last row sees 2048 keys or more runs on the CTA-pair kernel:
+    clusters of two CTAs over pairs of row tiles."""
+    x = S.make_prefill(1, 24, 4, 2048, seed=7)
+    q, k, v, g = (t.to(DEV) for t in (x.q, x.k, x.v, x.g))
+    G.prefill(q, k, v, g, kv_offset=0)
+    torch.cuda.synchronize()
+    rec = G.launch_log(1)[0]
+    R = 128 // 6
+    n_rtiles = -(-2048 // R)
+    assert rec["kernel"] == "attn_pair_kernel<prefill,bf16>"
+    assert rec["grid"] == 2 * ((n_rtiles + 1) // 2) * 4 and rec["block"] == 320
+
+
 def test_decode_launches_are_logged_in_order():
     x = S.make_decode(4, 24, 4, [1] * 4, [900, 50, 3000, 128], seed=6)
     q, kc, vc, g = (t.to(DEV) for t in (x.q, x.k_cache, x.v_cache, x.g))

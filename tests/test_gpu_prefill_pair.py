@@ -1,0 +1,82 @@
+"""gqa_attn_prefill_pair: the prefill computed by CTA pairs (tcgen05 .cta_group::2;
+two CTAs of a cluster take two row tiles of a KV group and share every K/V tile).
+
+Checked against the float64 oracle at the parity bar on shapes that cover an odd
+number of row tiles (the last pair's second tile is empty), GQA 1 / 6 / 8 / 16, an
+offset, several batches, a gate-less call and lse; against gqa_attn_prefill (the
+one-CTA form) within the same bar; and with NaN / Inf V values at keys that some rows
+of a pair do not see (the cleaning pass in pair form), where every element no planted
+value can reach keeps the clean run's bits and the non-finite pattern is the oracle's."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_head_gated_gb300 as G
+import oracle
+from synth import inputs as S
+from tests.parity import assert_nonfinite_parity, assert_parity, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+SHAPES = {
+    "gqa6_odd_tiles": (1, 24, 4, 300, 0),      # 15 row tiles: the last pair has one
+    "gqa1": (1, 4, 4, 300, 0),
+    "gqa8_offset_b2": (2, 16, 2, 257, 143),
+    "gqa16_short": (1, 16, 1, 9, 0),           # one row tile: its pair partner is empty
+    "gqa6_one_key_tile": (1, 24, 4, 128, 0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_pair_prefill_matches_oracle(name):
+    B, Hq, Hkv, Lq, off = SHAPES[name]
+    x = S.make_prefill(B, Hq, Hkv, Lq, Lkv=Lq + off, kv_offset=off, seed=21)
+    q, k, v, g = (t.to(DEV) for t in (x.q, x.k, x.v, x.g))
+    out, lse = G.prefill_pair(q, k, v, g, kv_offset=off, return_lse=True)
+    assert G.last_device_status() == 0
+    assert G.launch_log(1)[0]["kernel"] == "attn_pair_kernel<prefill,bf16>"
+    ref, r_lse = oracle.prefill(to_f64(x.q), to_f64(x.k), to_f64(x.v), to_f64(x.g), kv_offset=off)
+    assert_parity(out, ref, f"pair {name}")
+    assert_parity(lse, r_lse, f"pair lse {name}", max_abs=2e-3, median_rel=1.0)
+    one = G.prefill(q, k, v, g, kv_offset=off)
+    assert_parity(out, to_f64(one), f"pair vs one-CTA {name}")
+
+
+def test_pair_prefill_without_gate():
+    x = S.make_prefill(1, 24, 4, 200, seed=22)
+    q, k, v = (t.to(DEV) for t in (x.q, x.k, x.v))
+    out = G.prefill_pair(q, k, v, None)
+    assert G.last_device_status() == 0
+    ref, _ = oracle.prefill(to_f64(x.q), to_f64(x.k), to_f64(x.v), None, kv_offset=0)
+    assert_parity(out, ref, "pair, no gate")
+
+
+def test_pair_prefill_nonfinite_values_at_partially_masked_keys():
+    """NaN / Inf V elements at keys that some rows of a pair see and others do not
+    (its diagonal spans both CTAs' rows), and one NaN K value: the cleaning pass."""
+    B, Hq, Hkv, Lq, off = 1, 24, 4, 300, 64
+    x = S.make_prefill(B, Hq, Hkv, Lq, Lkv=Lq + off, kv_offset=off, seed=23)
+    q, g = x.q.to(DEV), x.g.to(DEV)
+    clean = G.prefill_pair(q, x.k.to(DEV), x.v.to(DEV), g, kv_offset=off)
+    plants = [("v", 0, 80, 3, float("nan")), ("v", 1, 100, 200, float("inf")),
+              ("v", 2, 140, 128, float("-inf")), ("v", 3, 330, 255, float("nan")),
+              ("k", 3, 200, 9, float("nan"))]
+    for kind, gk, key, col, val in plants:
+        (x.k if kind == "k" else x.v)[0, gk, key, col] = val
+    out = G.prefill_pair(q, x.k.to(DEV), x.v.to(DEV), g, kv_offset=off)
+    assert G.last_device_status() == 0
+    ref, _ = oracle.prefill(to_f64(x.q), to_f64(x.k), to_f64(x.v), to_f64(x.g), kv_offset=off)
+    assert not np.isfinite(ref).all()
+    assert_nonfinite_parity(out, ref, "pair non-finite")
+    gqa = Hq // Hkv
+    aff = np.zeros((B, Hq, Lq, 256), dtype=bool)
+    for kind, gk, key, col, _ in plants:
+        for h in range(gk * gqa, (gk + 1) * gqa):
+            rows = np.arange(Lq)[off + np.arange(Lq) >= key]
+            if kind == "k":
+                aff[0, h, rows, :] = True
+            else:
+                aff[0, h, rows, col] = True
+    keep = torch.from_numpy(~aff).to(DEV)
+    assert torch.equal(out[keep], clean[keep])
