@@ -80,3 +80,36 @@ def test_pair_prefill_nonfinite_values_at_partially_masked_keys():
                 aff[0, h, rows, col] = True
     keep = torch.from_numpy(~aff).to(DEV)
     assert torch.equal(out[keep], clean[keep])
+
+
+def test_pair_masked_future_keys_bit_exact():
+    """Perturbing keys a row does not see (but later rows of its pair do) leaves that
+    row bit for bit unchanged on CTA pairs too; 1000 rows put key 600 inside a pair."""
+    x = S.make_prefill(1, 24, 4, 1000, seed=24)
+    q, g = x.q.to(DEV), x.g.to(DEV)
+    a = G.prefill_pair(q, x.k.to(DEV), x.v.to(DEV), g)
+    x.k[:, :, 600:] = (x.k[:, :, 600:].float() * -3 + 1).to(torch.bfloat16)
+    x.v[:, :, 600:] = (x.v[:, :, 600:].float() * 5).to(torch.bfloat16)
+    b = G.prefill_pair(q, x.k.to(DEV), x.v.to(DEV), g)
+    assert G.last_device_status() == 0
+    assert torch.equal(a[:, :, :600], b[:, :, :600])
+    assert not torch.equal(a[:, :, 600:], b[:, :, 600:])
+
+
+def test_pair_long_prompt_routing_matches_oracle_sampled():
+    """gqa_attn_prefill on a prompt long enough for CTA pairs (3000 rows at an offset of
+    500 keys): sampled rows against the oracle, and the same bits as forcing the pair."""
+    B, Hq, Hkv, Lq, off = 1, 16, 2, 3000, 500
+    x = S.make_prefill(B, Hq, Hkv, Lq, Lkv=Lq + off, kv_offset=off, seed=25)
+    q, k, v, g = (t.to(DEV) for t in (x.q, x.k, x.v, x.g))
+    out = G.prefill(q, k, v, g, kv_offset=off)
+    assert G.launch_log(1)[0]["kernel"] == "attn_pair_kernel<prefill,bf16>"
+    forced = G.prefill_pair(q, k, v, g, kv_offset=off)
+    assert torch.equal(out, forced)
+    gen = np.random.default_rng(25)
+    rows = [(0, int(h), int(i)) for h, i in zip(gen.integers(0, Hq, 48), gen.integers(0, Lq, 48))]
+    rows += [(0, 0, 0), (0, Hq - 1, Lq - 1), (0, 3, 1535), (0, 9, 1536)]
+    ref, _ = oracle.prefill(to_f64(x.q), to_f64(x.k), to_f64(x.v), to_f64(x.g), kv_offset=off,
+                            rows=rows)
+    got = torch.stack([out[b_, h, i] for b_, h, i in rows])
+    assert_parity(got, ref, "routed pair, sampled rows")
