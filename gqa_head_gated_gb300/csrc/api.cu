@@ -60,10 +60,13 @@ bool make_ctl(LaunchCtl* ctl) {
 
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
-// Decode / verify groups with at least this many packed rows (new rows x query heads
-// per KV group) run on the tcgen05 kernel; fewer run on the mma.sync split kernel,
-// which is memory-bound there already.
-constexpr long long kTcMinPackedRows = 64;
+// Decode / verify groups with more than 16 packed rows (new rows x query heads per KV
+// group) run on the tcgen05 kernel; up to 16 on the mma.sync split kernel, in its
+// 16-row form with two CTAs per SM.  Measured on GB300 (one-call decode, L2 flushed):
+// from 18 packed rows on the tcgen05 split is 1.15-1.8x faster (the mma.sync kernel's
+// 32- and 64-row forms run one CTA per SM); from 6 to 16 the two are within ~10 %,
+// the mma.sync kernel ahead on the 27B decode.
+constexpr long long kTcMinPackedRows = 17;
 constexpr int kTcMinSplitKeys = 1024;   // at least 8 key tiles per tcgen05 CTA
 
 bool tc_path(int Hq, int Hkv, int max_rows) {
@@ -130,8 +133,8 @@ size_t workspace_bytes_for(int T, int Hq, int S) {
   return size_t(S) * rows * 256 * sizeof(float) + size_t(S) * rows * sizeof(float);
 }
 
-// The one-call decode's choice: the mma.sync kernel (fewer than 64 packed rows per
-// KV group) runs balanced shares when the batch fits the kernel's table.
+// The one-call decode's choice: the mma.sync kernel (at most 16 packed rows per KV
+// group) runs balanced shares when the batch fits the kernel's table.
 bool use_balanced(int B, int Hq, int Hkv, int max_rows) {
   return !tc_path(Hq, Hkv, max_rows) && B <= kBalancedMaxSeqs;
 }

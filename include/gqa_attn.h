@@ -185,14 +185,14 @@ int gqa_attn_decode_plan(int B, int T, int Hq, int Hkv, int max_rows, int max_kv
  * num_splits >= 1 and split_keys (a positive multiple of 64) with
  * num_splits*split_keys >= max_kv_len; gqa_attn_decode_plan() gives the defaults.
  * split_keys = 0 selects balanced shares (the form gqa_attn_decode uses on the
- * mma.sync path, i.e. fewer than 64 packed rows per group, with B <= 256;
+ * mma.sync path, i.e. at most 16 packed rows per group, with B <= 256;
  * otherwise GQA_ERR_UNSUPPORTED): the keys of all (sequence, KV group, row block)
  * ranges are laid end to end in 32-key tiles and cut into equal shares, one per
  * resident CTA, so ragged lengths cost no tail; a range split among k CTAs gets
  * parts 0..k-1 and lse -inf in parts k..num_splits-1.  num_splits >= 3 is then the
  * part capacity per row (gqa_attn_decode uses 16); the shares are never cut so
  * finely that a range needs more.
- * Kernel: when a KV group packs at least 64 rows (max_rows x Hq/Hkv >= 64) and
+ * Kernel: when a KV group packs more than 16 rows (max_rows x Hq/Hkv >= 17) and
  * split_keys is a multiple of 128, the split runs on tcgen05 tensor cores (TMEM
  * accumulators, TMA-staged tiles); otherwise on an mma.sync kernel with 16-byte
  * cp.async cache reads.  Both give the same partial results up to rounding.

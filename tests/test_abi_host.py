@@ -119,7 +119,8 @@ def test_split_rejects_bad_plan(lib):
     assert f(*args, 2, 448, None) == 1           # 2 * 448 < 1000 keys
     assert f(*args[:-3], 1024, 1, 1025, 2, 576, None) == 1   # max_kv_len > Lcap
     assert f(*args, 2, 0, None) == 1             # balanced shares need >= 3 part slots
-    # balanced shares are an mma.sync-path form: 32 rows x GQA 2 = 64 packed rows is not
+    # balanced shares are an mma.sync-path form: 32 rows x GQA 2 = 64 packed rows
+    # (more than 16) is not
     assert f(P(16), P(32), P(48), P(80), P(96), P(112), P(128), 2, 64, 4, 2, 1024, 32, 1000,
              16, 0, None) == 2
 
@@ -139,9 +140,9 @@ def test_decode_plan_rule(lib):
         assert C % 64 == 0 and C >= 64
         assert S >= 1 and S * C >= L and (S - 1) * C < L        # no empty trailing split
         size = lib.gqa_attn_decode_workspace_size(B, T, Hq, Hkv, R, L)
-        # fewer than 64 packed rows per group and B <= 256: the one-call decode runs
+        # at most 16 packed rows per group and B <= 256: the one-call decode runs
         # balanced shares with 16 part slots per row; otherwise the plan's S
-        parts = 16 if R * (Hq // Hkv) < 64 and B <= 256 else S
+        parts = 16 if R * (Hq // Hkv) <= 16 and B <= 256 else S
         assert size == parts * T * Hq * 257 * 4
     assert plan(lib, 16, 16, 24, 4, 1, 32768)[1:] == (15, 2240)    # 6 x 152 CTAs / 64 units
     # 32 rows x 8 heads per group: tcgen05 path, 3 x 152 CTAs / (8 x 2 x 2 row tiles),

@@ -59,7 +59,8 @@ SWEEP = [
     (24, 4, [1, 1], [8192, 8193]),
     (16, 2, [3, 4, 8], [3, 100, 4097]),
     (16, 2, [16, 32], [40, 1000]),
-    (12, 1, [5, 2], [700, 5]),                # GQA 12: 60 packed rows
+    (12, 1, [5, 2], [700, 5]),                # GQA 12: 60 packed rows (tcgen05)
+    (16, 2, [2, 1, 2], [900, 50, 3000]),      # 16 packed rows: the mma.sync kernel's largest
     (32, 4, [32, 7], [300, 3000]),            # GQA 8 x 32 rows = 256 packed rows
     (6, 6, [64], [2000]),                     # 64 rows, GQA 1
     (16, 1, [9, 0, 1], [500, 0, 33]),         # a sequence with no rows
@@ -137,7 +138,7 @@ def test_split_then_merge_equals_decode():
                                          (24, 4, [11, 2], [4097, 700]),
                                          (64, 1, [2, 1], [1000, 5000])])
 def test_tc_and_mma_split_paths_agree(Hq, Hkv, rows, kv):
-    """Groups of >= 64 packed rows take the tcgen05 split kernel when the split size
+    """Groups of more than 16 packed rows take the tcgen05 split kernel when the split size
     is a multiple of 128 and the mma.sync kernel otherwise: both match the oracle and
     each other."""
     x = S.make_decode(len(rows), Hq, Hkv, rows, kv, seed=sum(kv))
@@ -279,7 +280,7 @@ def test_balanced_shares_extreme_lengths(lens):
     ([64, 2], [70, 64000]),                           # 64 rows over a short cache
 ])
 def test_tcgen05_path_extreme_lengths(rows, lens):
-    """Verify rows on the tcgen05 split kernel (>= 64 packed rows per group) with
+    """Verify rows on the tcgen05 split kernel (more than 16 packed rows per group) with
     extreme length mixes, chain and tree masks, against the oracle."""
     B = len(rows)
     x = S.make_decode(B, 16, 2, rows, lens, Lcap=max(lens) + 5, seed=sum(lens) % 1000)

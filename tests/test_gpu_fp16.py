@@ -110,7 +110,8 @@ def test_decode_27b_fp16_workload():
     (24, 4, [1, 1, 1], [8191, 300, 129]),       # mma.sync split
     (16, 2, [3, 4, 8], [3, 100, 4097]),          # tcgen05 split (64 packed rows)
     (16, 2, [16, 32], [40, 3000]),               # tcgen05 split (256 packed rows)
-    (12, 1, [5, 2], [700, 5]),                   # mma.sync (60 packed rows)
+    (12, 1, [5, 2], [700, 5]),                   # tcgen05 split (60 packed rows)
+    (16, 2, [2, 1], [700, 5]),                   # mma.sync (16 packed rows)
 ])
 def test_decode_fp16_sweep(Hq, Hkv, rows, kv):
     x = S.make_decode(len(rows), Hq, Hkv, rows, kv, Lcap=max(kv) + 5, seed=sum(kv) + 3,

@@ -107,12 +107,12 @@ VERIFY = {
     "tc": ((3, 16, 2, [8, 16, 1], [3000, 700, 129], 3100),
            [(0, "v_inf", 1, 2994, 3), (0, "v_nan", 0, 2999, 100), (1, "v_ninf", 1, 690, 200),
             (1, "k_nan", 0, 699, 1), (1, "v_inf", 0, 685, 50)]),
-    # 4 / 2 new rows x GQA 8: mma.sync kernel, balanced shares
-    "mma": ((3, 16, 2, [4, 2, 1], [3000, 700, 129], 3100),
+    # 2 / 2 / 1 new rows x GQA 8 (16 packed rows): mma.sync kernel, balanced shares
+    "mma": ((3, 16, 2, [2, 2, 1], [3000, 700, 129], 3100),
             [(0, "v_inf", 1, 2997, 3), (0, "v_nan", 0, 2999, 100), (1, "v_ninf", 1, 699, 200),
              (0, "k_nan", 1, 2998, 9)]),
-    # 5 / 3 new rows x GQA 6 (30 packed rows in a 32-row block)
-    "mma_gqa6": ((2, 24, 4, [5, 3], [1500, 900], 1600),
+    # 2 / 2 new rows x GQA 6 (12 packed rows in a 16-row block)
+    "mma_gqa6": ((2, 24, 4, [2, 2], [1500, 900], 1600),
                  [(0, "v_inf", 3, 1497, 77), (0, "v_ninf", 2, 1499, 78), (1, "v_nan", 1, 898, 79),
                   (1, "k_nan", 0, 899, 80)]),
 }

@@ -33,11 +33,13 @@ def ref_tree(x, masks):
 
 
 CASES = [
-    # Hq, Hkv, rows, kv_lens: >= 64 packed rows per group take the tcgen05 kernel
+    # Hq, Hkv, rows, kv_lens: more than 16 packed rows per group take the tcgen05 kernel
     (16, 2, [8, 3, 16, 1], [3000, 700, 9000, 129]),     # tcgen05 (16 x 8 = 128)
-    (8, 4, [5, 12], [2000, 4100]),                       # mma.sync (12 x 2 = 24)
+    (8, 4, [5, 12], [2000, 4100]),                       # tcgen05 (12 x 2 = 24)
     (4, 4, [64, 7], [5000, 64]),                         # tcgen05, a 64-row tree
-    (24, 4, [9, 2, 4], [300, 8200, 1000]),               # mma.sync (9 x 6 = 54)
+    (24, 4, [9, 2, 4], [300, 8200, 1000]),               # tcgen05 (9 x 6 = 54)
+    (8, 4, [5, 8], [2000, 4100]),                        # mma.sync (8 x 2 = 16)
+    (24, 4, [2, 2, 1], [300, 8200, 1000]),               # mma.sync (2 x 6 = 12)
 ]
 
 
@@ -109,7 +111,7 @@ def _random_verify(n, seed):
 
 
 @pytest.mark.parametrize("Hq,Hkv,rows,kv", _random_verify(8, 77) + [
-    (4, 2, [3, 9, 0, 5], [100, 5000, 0, 37]),        # mma.sync path, a sequence with no rows
+    (4, 2, [3, 8, 0, 5], [100, 5000, 0, 37]),        # mma.sync path, a sequence with no rows
     (6, 3, [1, 1, 1], [1, 4097, 300])])               # decode rows, a one-key sequence
 def test_random_tree_and_chain_verify(Hq, Hkv, rows, kv):
     x = S.make_decode(len(rows), Hq, Hkv, rows, kv, Lcap=max(kv) + 17, seed=sum(kv) + Hq)

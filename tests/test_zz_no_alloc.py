@@ -4,7 +4,7 @@ plug-in whose host application only hands it fixed buffers).  It is gqa_attn_dec
 with a fixed 16 MiB area owned by the library as its workspace.
 
 The test calls it through the C ABI on each of the one-call decode's paths (tcgen05
-split kernel; mma.sync kernel with balanced shares, at the size where the area is
+split kernel; mma.sync kernel with balanced shares, near the size where the area is
 just enough; mma.sync kernel with fixed splits for a batch past the balanced table)
 and checks every output against the float64 oracle at the parity bar, and bit for
 bit (out and lse) against gqa_attn_decode with a caller workspace.  Each shape is
@@ -49,8 +49,9 @@ def _lens(n, lo, hi, seed):
 SHAPES = {
     # 8 new rows x GQA 8 = 64 packed rows: the tcgen05 split kernel
     "tc_split": (3, 16, 2, [1, 3, 8], [3000, 500, 7000]),
-    # 31 rows x GQA 1: balanced shares whose 16 part slots take 16.3 MB of the area
-    "balanced_at_limit": (1, 32, 32, [31], [1500]),
+    # one row x GQA 16 over 15 sequences: balanced shares whose 16 part slots take
+    # 15.8 MB of the area
+    "balanced_near_limit": (15, 64, 4, [1] * 15, _lens(15, 200, 1500, 9)),
     # 300 sequences (past the balanced table's 256): fixed splits on the mma.sync kernel
     "fixed_split": (300, 16, 2, [1] * 300, _lens(300, 40, 400, 7)),
 }
