@@ -28,9 +28,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmO = 0;
 constexpr uint32_t kTmS = 256;                // S buffer b at kTmS + kN*b
 // Lazy-rescale threshold in log2 units: P <= 2^threshold must fit the element type
-// (bf16: 2^32, fp16: 2^8, below its 65504 maximum).
+// (bf16: 2^32; fp16: 2^15 = 32768, below its 65504 maximum).  l and O are fp32.
 template <bool kF16>
-__device__ __forceinline__ float rescale_threshold() { return kF16 ? 8.0f : 32.0f; }
+__device__ __forceinline__ float rescale_threshold() { return kF16 ? 15.0f : 32.0f; }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -373,8 +373,8 @@ int gqa_attn_mask_check(int B, int Hq, int Hkv, int Lq, int Lkv, int mask_kind,
  * bf16 entry point of the same name without `_f16`; Q, K/Kcache, V/Vcache, G and
  * out are fp16 (IEEE binary16) instead of bf16.  P enters the P.V product as
  * fp16; the tensor-core kernels rescale a row's running sum whenever its maximum
- * grows by more than 8 in log2 units, so every P stays at or below 2^8, inside
- * fp16's range (bf16 uses 32).  Scores, softmax sums and accumulation stay fp32.
+ * grows by more than 15 in log2 units, so every P stays at or below 2^15 = 32768,
+ * inside fp16's range (bf16 uses 32).  Scores, softmax sums and accumulation stay fp32.
  * Partial results (O_parts, lse_parts) are fp32 in both types.  gqa_kv_append
  * and gqa_kv_keep copy 16-bit elements and serve both types unchanged.
  */

@@ -50,8 +50,9 @@ def test_prefill_fp16_shapes(B, Hq, Hkv, Lq, Lkv, off):
 def test_prefill_fp16_rescale_stress():
     """Keys scaled x8 (2% of rows) give score spreads of tens of log2 units, so the
     running maximum jumps past the rescale threshold again and again.  fp16 P must
-    stay finite: the tcgen05 kernel rescales once the maximum grows by 8 (P <= 2^8);
-    with bf16's threshold of 32 P would reach 2^32 and overflow fp16."""
+    stay finite: the tcgen05 kernel rescales once the maximum grows by 15 (P <= 2^15,
+    below fp16's 65504); with bf16's threshold of 32 P would reach 2^32 and overflow
+    fp16."""
     x = S.make_prefill(1, 8, 2, 700, seed=31, outlier_frac=0.02, dtype=F16)
     out = prefill_run(x)
     assert torch.isfinite(out).all()
