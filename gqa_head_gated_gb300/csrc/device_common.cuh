@@ -103,12 +103,55 @@ __device__ __forceinline__ float nonfinite_acc_f32(float acc, float x) {
   return r;
 }
 
-// Logistic function for the output gate, fp32.  The approximate divide has no
-// branch to an IEEE slow path, so a thread's 128 gates interleave; its error (a few
-// fp32 ulp, like __expf's) is far below the one rounding of the output to bf16/fp16.
-// g = -inf or < -88 gives exactly 0 (1/inf), g = +inf gives 1, NaN stays NaN.
+// Logistic function for the output gate, fp32: 1 / (1 + 2^(-g log2 e)), from the
+// approximate flush-to-zero ex2 and rcp instructions directly (one multiply, one
+// add, two multi-function-unit operations, no range fix-ups), so a thread's 128
+// gates interleave and the gate epilogue issues few instructions.  Its error (a few
+// fp32 ulp, from the two approximations) is far below the one rounding of the output
+// to bf16 / fp16.  g = +inf gives 1 (2^-inf = 0); g = -inf, or g below about -87.3,
+// gives 0 (1 + 2^x >= 2^126, whose reciprocal is below fp32's smallest normal and is
+// flushed); a NaN gate stays NaN.
 __device__ __forceinline__ float gate_sigmoid(float g) {
-  return __fdividef(1.0f, 1.0f + __expf(-g));
+  float e, s;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(s) : "f"(1.0f + e));
+  return s;
+}
+
+// Two gates at once, with the multiplies and adds as packed fp32 pairs (the same
+// per-element operations as gate_sigmoid).
+__device__ __forceinline__ float2 gate_sigmoid2(float g0, float g1) {
+  float s0, s1;
+  asm("{\n\t"
+      ".reg .b64 x, c, d;\n\t"
+      ".reg .f32 x0, x1, e0, e1;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 c, {%4, %4};\n\t"
+      "mul.rn.f32x2 x, x, c;\n\t"
+      "mov.b64 {x0, x1}, x;\n\t"
+      "ex2.approx.ftz.f32 e0, x0;\n\t"
+      "ex2.approx.ftz.f32 e1, x1;\n\t"
+      "mov.b64 x, {e0, e1};\n\t"
+      "mov.b64 c, {%5, %5};\n\t"
+      "add.rn.f32x2 d, x, c;\n\t"
+      "mov.b64 {x0, x1}, d;\n\t"
+      "rcp.approx.ftz.f32 %0, x0;\n\t"
+      "rcp.approx.ftz.f32 %1, x1;\n\t"
+      "}" : "=f"(s0), "=f"(s1) : "f"(g0), "f"(g1), "f"(-1.4426950408889634f), "f"(1.0f));
+  return make_float2(s0, s1);
+}
+
+// (a.x * b.x, a.y * b.y) as one packed fp32 multiply.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float x, y;
+  asm("{\n\t"
+      ".reg .b64 p, q;\n\t"
+      "mov.b64 p, {%2, %3};\n\t"
+      "mov.b64 q, {%4, %5};\n\t"
+      "mul.rn.f32x2 p, p, q;\n\t"
+      "mov.b64 {%0, %1}, p;\n\t"
+      "}" : "=f"(x), "=f"(y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return make_float2(x, y);
 }
 
 }  // namespace gqa

@@ -564,13 +564,14 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             uint32_t r[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              float2 gs = make_float2(1.f, 1.f);
+              float2 res = mul2(make_float2(__uint_as_float(o[v * 8 + 2 * e]),
+                                            __uint_as_float(o[v * 8 + 2 * e + 1])),
+                                make_float2(inv_l, inv_l));
               if (p.G != nullptr) {
                 const float2 f = unpack_elem2<kF16>(w[e]);
-                gs = make_float2(gate_sigmoid(f.x), gate_sigmoid(f.y));
+                res = mul2(res, gate_sigmoid2(f.x, f.y));
               }
-              r[e] = pack_elem2<kF16>(__uint_as_float(o[v * 8 + 2 * e]) * inv_l * gs.x,
-                                      __uint_as_float(o[v * 8 + 2 * e + 1]) * inv_l * gs.y);
+              r[e] = pack_elem2<kF16>(res.x, res.y);
             }
             *reinterpret_cast<uint4*>(stage + off) = make_uint4(r[0], r[1], r[2], r[3]);
           }
