@@ -141,6 +141,33 @@ __device__ __forceinline__ float2 gate_sigmoid2(float g0, float g1) {
   return make_float2(s0, s1);
 }
 
+// (a.x * b.x + c.x, a.y * b.y + c.y) as one packed fp32 fma.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float x, y;
+  asm("{\n\t"
+      ".reg .b64 pa, pb, pc;\n\t"
+      "mov.b64 pa, {%2, %3};\n\t"
+      "mov.b64 pb, {%4, %5};\n\t"
+      "mov.b64 pc, {%6, %7};\n\t"
+      "fma.rn.f32x2 pa, pa, pb, pc;\n\t"
+      "mov.b64 {%0, %1}, pa;\n\t"
+      "}" : "=f"(x), "=f"(y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return make_float2(x, y);
+}
+
+// (a.x + b.x, a.y + b.y) as one packed fp32 add.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float x, y;
+  asm("{\n\t"
+      ".reg .b64 pa, pb;\n\t"
+      "mov.b64 pa, {%2, %3};\n\t"
+      "mov.b64 pb, {%4, %5};\n\t"
+      "add.rn.f32x2 pa, pa, pb;\n\t"
+      "mov.b64 {%0, %1}, pa;\n\t"
+      "}" : "=f"(x), "=f"(y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return make_float2(x, y);
+}
+
 // (a.x * b.x, a.y * b.y) as one packed fp32 multiply.
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   float x, y;

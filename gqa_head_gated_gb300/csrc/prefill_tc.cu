@@ -805,16 +805,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           continue;  // the next exchange stops both threads of the pair
         }
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t pk[kHalf / 2];
+        const float2 sc2 = make_float2(kScaleLog2, kScaleLog2);
+        const float2 ms2 = make_float2(-msub, -msub);
 #pragma unroll
         for (int c = 0; c < kHalf / 2; ++c) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), kScaleLog2, -msub));
-          const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), kScaleLog2, -msub));
-          ls4[c & 3] += p0 + p1;
+          const float2 x = fma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
+                                sc2, ms2);
+          const float p0 = ex2(x.x);
+          const float p1 = ex2(x.y);
+          ls2[c & 1] = add2(ls2[c & 1], make_float2(p0, p1));
           pk[c] = pack_elem2<kF16>(p0, p1);
         }
-        l_part += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+        l_part += (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
         const uint32_t pdst = trow + kTmS + uint32_t(kN) * buf + uint32_t(kHalf) * half;
         if constexpr (kHalf == 64) {
           ptx::tmem_st32_wait(pdst, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
