@@ -185,6 +185,32 @@ template <int kKind, typename E, int kN_>
 __device__ __forceinline__ void apply_mask_row_smem(uint32_t (&s)[kN_], const E* row, int key0,
                                                     int lim) {
   constexpr int kVec = 16 / int(sizeof(E));
+  static_assert(kVec % 2 == 0, "keys go in pairs");
+  if (key0 + kN_ <= lim) {
+    // Every key of the row's share is causally visible: no per-key check.  A bool
+    // mask selects; an additive one moves pairs of scores by one packed fma.
+#pragma unroll
+    for (int c0 = 0; c0 < kN_; c0 += kVec) {
+      const uint4 u = *reinterpret_cast<const uint4*>(row + c0);
+      const E* e = reinterpret_cast<const E*>(&u);
+#pragma unroll
+      for (int v = 0; v < kVec; v += 2) {
+        if constexpr (kKind == 1) {
+          if (!e[v]) s[c0 + v] = __float_as_uint(-INFINITY);
+          if (!e[v + 1]) s[c0 + v + 1] = __float_as_uint(-INFINITY);
+        } else {
+          const float a0 = mask_elem<kKind>(e[v]);
+          const float a1 = mask_elem<kKind>(e[v + 1]);
+          const float2 x = fma2(make_float2(16.f, 16.f), make_float2(a0, a1),
+                                make_float2(__uint_as_float(s[c0 + v]),
+                                            __uint_as_float(s[c0 + v + 1])));
+          s[c0 + v] = __float_as_uint(a0 == -INFINITY ? -INFINITY : x.x);
+          s[c0 + v + 1] = __float_as_uint(a1 == -INFINITY ? -INFINITY : x.y);
+        }
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int c0 = 0; c0 < kN_; c0 += kVec) {
     const uint4 u = *reinterpret_cast<const uint4*>(row + c0);
