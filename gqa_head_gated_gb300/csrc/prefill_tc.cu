@@ -799,8 +799,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         ok = mine && sm.ok[buf][half ^ 1][row];
         if (!ok) break;
         const float tmax = fmaxf(mx, sm.red[buf][half ^ 1][row]);
-        bool rescale = false;   // O is multiplied by alpha once P_j is stored
-        float alpha = 1.f;
+        bool store_ok = true;
         if (j == 0) {
           m_run = tmax;
         } else if (__any_sync(0xffffffffu, tmax > m_run + rescale_threshold<kF16>())) {
@@ -809,10 +808,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           // rose past the threshold move it; the others multiply by exactly 1, so every
           // row's result depends on its own scores alone.
           const bool need = tmax > m_run + rescale_threshold<kF16>();
-          alpha = need ? ex2(m_run - tmax) : 1.f;
+          const float alpha = need ? ex2(m_run - tmax) : 1.f;
           if (need) m_run = tmax;
           l_part *= alpha;
-          rescale = true;
+          // O must hold PV_{j-1} before it is rescaled.
+          store_ok = warp_all(ptx::mbar_wait(&sm.pv_done, (J - 1) & 1, tmo, &sm.abort));
+          if (store_ok) {
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+              uint32_t o[32];
+              const uint32_t ta = trow + kTmO + 128u * half + 32u * cc;
+              ptx::tmem_ld32_wait(ta, o);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              ptx::tmem_st32_wait(ta, o);
+            }
+          }
+        }
+        if (!store_ok) {
+          fail(sm, p);
+          continue;  // the next exchange stops both threads of the pair
         }
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
         float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -834,26 +850,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           ptx::tmem_st32_wait(pdst, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
         } else {
           ptx::tmem_st16_wait(pdst, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        }
-        if (rescale) {
-          // O must hold PV_{j-1} before it is rescaled; P_j, in its own buffer, was
-          // computed and stored while that product ran.
-          const bool store_ok =
-              warp_all(ptx::mbar_wait(&sm.pv_done, (J - 1) & 1, tmo, &sm.abort));
-          if (!store_ok) {
-            fail(sm, p);
-            continue;  // the next exchange stops both threads of the pair
-          }
-          ptx::tc_fence_after();
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t o[32];
-            const uint32_t ta = trow + kTmO + 128u * half + 32u * cc;
-            ptx::tmem_ld32_wait(ta, o);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            ptx::tmem_st32_wait(ta, o);
-          }
         }
         if constexpr (kClean) {
           // Once V_j is cleaned: for its hit keys among this thread's keys, record
