@@ -6,6 +6,7 @@
     single row, land on the expected kernel and match the oracle.
   * Prompts of 8191 and 8193 rows end one key before and one key past the 64th
     128-key tile.
+  Both in bf16 and in fp16 (the fp16 results also meet the fp16 bar).
   * A 3000-row prompt run in chunks whose last rows see 1024, 2047, 2048 and 3000
     keys (single CTAs for the first two, pairs for the rest) equals the whole-prompt
     run: the prompt-row frames of the pages' prefill are cut at such seams."""
@@ -16,12 +17,19 @@ import torch
 import gqa_head_gated_gb300 as G
 import oracle
 from synth import inputs as S
-from tests.parity import assert_parity, errors, to_f64
+from tests.parity import assert_parity, assert_parity_dtype, errors, to_f64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 SINGLE = "attn_tc_kernel<prefill,bf16>"
 PAIR = "attn_pair_kernel<prefill,bf16>"
+DTYPES = [torch.bfloat16, torch.float16]
+IDS = ["bf16", "fp16"]
+
+
+def _names(dtype):
+    sfx = "fp16>" if dtype == torch.float16 else "bf16>"
+    return "attn_tc_kernel<prefill," + sfx, "attn_pair_kernel<prefill," + sfx
 
 
 def _rows(Hq, Lq, n, seed, extra=()):
@@ -39,7 +47,7 @@ def _check_sampled(x, out, lse, rows, what):
     r_out, r_lse = oracle.prefill(to_f64(x.q), to_f64(x.k), to_f64(x.v), to_f64(x.g),
                                   kv_offset=x.kv_offset, rows=rows)
     got = torch.stack([out[b, h, i] for b, h, i in rows])
-    assert_parity(got, r_out, what)
+    assert_parity_dtype(got, r_out, what)
     got_lse = np.array([float(lse[b, h, i]) for b, h, i in rows])
     np.testing.assert_allclose(got_lse, r_lse, rtol=0, atol=2e-3)
 
@@ -54,20 +62,24 @@ def _run(x):
 
 @pytest.mark.parametrize("Lq,off", [(2047, 0), (2048, 0), (2049, 0),
                                     (1, 2046), (1, 2047), (300, 1748), (301, 1748)])
-def test_pair_routing_threshold(Lq, off):
-    x = S.make_prefill(1, 8, 1, Lq, kv_offset=off, seed=Lq + off)
+@pytest.mark.parametrize("dtype", DTYPES, ids=IDS)
+def test_pair_routing_threshold(dtype, Lq, off):
+    single, pair = _names(dtype)
+    x = S.make_prefill(1, 8, 1, Lq, kv_offset=off, seed=Lq + off, dtype=dtype)
     out, lse, kernel = _run(x)
-    assert kernel == (PAIR if off + Lq >= 2048 else SINGLE), kernel
+    assert out.dtype == dtype
+    assert kernel == (pair if off + Lq >= 2048 else single), kernel
     rows = _rows(8, Lq, 48, Lq, extra=(15, 16, 31, 32, Lq - 2, Lq - 17))
     _check_sampled(x, out, lse, rows, f"Lq {Lq} at offset {off}")
 
 
 @pytest.mark.parametrize("Lq", [8191, 8193])
 @pytest.mark.parametrize("Hq,Hkv", [(8, 1), (4, 4)], ids=["gqa8", "gqa1"])
-def test_long_prompt_key_tile_edge(Lq, Hq, Hkv):
-    x = S.make_prefill(1, Hq, Hkv, Lq, seed=Lq * Hq)
+@pytest.mark.parametrize("dtype", DTYPES, ids=IDS)
+def test_long_prompt_key_tile_edge(dtype, Lq, Hq, Hkv):
+    x = S.make_prefill(1, Hq, Hkv, Lq, seed=Lq * Hq, dtype=dtype)
     out, lse, kernel = _run(x)
-    assert kernel == PAIR, kernel
+    assert kernel == _names(dtype)[1], kernel
     assert torch.isfinite(out).all()
     rows = _rows(Hq, Lq, 40, Lq, extra=(127, 128, 8063, 8064, 8190, 8191, 8192))
     _check_sampled(x, out, lse, rows, f"Lq {Lq}, {Hq}/{Hkv} heads")
