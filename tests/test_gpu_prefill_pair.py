@@ -2,11 +2,12 @@
 two CTAs of a cluster take two row tiles of a KV group and share every K/V tile).
 
 Checked against the float64 oracle at the parity bar on shapes that cover an odd
-number of row tiles (the last pair's second tile is empty), GQA 1 / 6 / 8 / 16, an
-offset, several batches, a gate-less call and lse; against gqa_attn_prefill (the
-one-CTA form) within the same bar; and with NaN / Inf V values at keys that some rows
-of a pair do not see (the cleaning pass in pair form), where every element no planted
-value can reach keeps the clean run's bits and the non-finite pattern is the oracle's."""
+number of row tiles (the last pair's second tile is empty), GQA 1 / 3 / 5 / 6 / 7 /
+8 / 16 / 32 / 128, an offset, several batches, a gate-less call and lse; against
+gqa_attn_prefill (the one-CTA form) within the same bar; and with NaN / Inf V values
+at keys that some rows of a pair do not see (the cleaning pass in pair form), where
+every element no planted value can reach keeps the clean run's bits and the
+non-finite pattern is the oracle's."""
 import numpy as np
 import pytest
 import torch
@@ -25,6 +26,12 @@ SHAPES = {
     "gqa8_offset_b2": (2, 16, 2, 257, 143),
     "gqa16_short": (1, 16, 1, 9, 0),           # one row tile: its pair partner is empty
     "gqa6_one_key_tile": (1, 24, 4, 128, 0),
+    # packings with empty MMA rows (128 not a multiple of GQA) and GQA 32 / 128
+    "gqa3": (1, 6, 2, 260, 0),                 # R = 42, 126 packed rows
+    "gqa5_offset": (1, 10, 2, 131, 60),        # R = 25, 125 packed rows
+    "gqa7": (1, 7, 1, 200, 0),                 # R = 18, 126 packed rows
+    "gqa32_b3": (3, 64, 2, 19, 5),             # R = 4
+    "gqa128": (1, 128, 1, 37, 0),              # R = 1: 37 row tiles, 19 pairs
 }
 
 
