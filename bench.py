@@ -600,6 +600,23 @@ def ours(args):
     pf_tflops = flops / (pf_avg / 1e3) / 1e12
     bf16_peak = float(peaks["bf16_tflops"])
     pf_e2e_avg = sum(pf_e2e) / len(pf_e2e)
+    # DRAM bytes of the prefill launch: the capture of this very workload when its
+    # record matches the kernel source, else the 4,096-row capture scaled by input bytes
+    pf_in_bytes = (pf.q.numel() + pf.k.numel() + pf.v.numel() + pf.g.numel()) * 2
+    pf_pair = bool(pf_launch and pf_launch["kernel"].startswith("attn_pair"))
+    pf_traffic = args.prefill_traffic
+    pf_traffic_note = "given on the command line"
+    if pf_traffic is None and pf_pair:
+        pf_traffic = dram_traffic("attn_pair_kernel_prefill_27b", pf_in_bytes)
+        pf_traffic_note = ("ncu capture of this workload's launch (bench.py --case prefill_27b, "
+                           "one pass, cold L2); output writes still in L2 when the kernel "
+                           "ended are not counted")
+    if pf_traffic is None and args.prefill_traffic is None:
+        pf_traffic = dram_traffic("attn_pair_kernel_prefill" if pf_pair
+                                  else "attn_tc_kernel_prefill", pf_in_bytes)
+        pf_traffic_note = ("not measured on this launch: the DRAM bytes of the 4,096-row "
+                           "capture, scaled by input bytes; output writes still in L2 when "
+                           "that kernel ended are not counted")
 
     # the other throughput workloads of the metric, inside the same line
     more = {}
@@ -856,16 +873,8 @@ def ours(args):
                              "achieved": round(pf_tflops, 2), "peak": bf16_peak,
                              "peak_source": f"{peak_src} bf16_tflops (burst)",
                              "unit": "TFLOP/s", "frac": round(pf_tflops / bf16_peak, 4),
-                             "traffic": args.prefill_traffic if args.prefill_traffic is not None
-                             else dram_traffic("attn_pair_kernel_prefill"
-                                               if pf_launch and pf_launch["kernel"].startswith("attn_pair")
-                                               else "attn_tc_kernel_prefill",
-                                               (pf.q.numel() + pf.k.numel() + pf.v.numel() +
-                                                pf.g.numel()) * 2),
-                             "traffic_note": "not measured on this launch: the DRAM bytes of "
-                                             "the 4,096-row capture, scaled by input bytes; "
-                                             "output writes still in L2 when that kernel "
-                                             "ended are not counted"},
+                             "traffic": pf_traffic,
+                             "traffic_note": pf_traffic_note},
                 "e2e": {"value": round(flops / (pf_e2e_avg / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                         "h2d_bytes_per_step": pf_h2d, "d2h_bytes_per_step": pf_d2h},
                 "device_status": pf_status,
@@ -942,6 +951,9 @@ CASES = {
     "masked_4k": lambda: S.make_prefill(1, 24, 4, 4096, seed=2, outlier_frac=0.01),
     # the 128-row prompt of the bench's tiny-prefill line (28 CTAs of one key tile)
     "prefill_tiny": lambda: S.tiny_prefill(),
+    # the 27B-shape prefill at full size (8192 causal rows, 24/4 heads, 320 MiB of
+    # Q/K/V/G/out, ~0.53 ms per launch): for single-pass DRAM counters only
+    "prefill_27b": lambda: S.WORKLOADS["prefill_27b"](),
 }
 
 
