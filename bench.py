@@ -817,6 +817,18 @@ def ours(args):
                          f"({secs:.1f} s)"}
 
     if rank == 0:
+        # DRAM bytes of the split launch: the capture of this very workload when its
+        # record matches the kernel source, else the 8K-key capture scaled by keys held
+        held = int(x.kv_lens.sum()) * x.k_cache.shape[1]
+        dec_traffic, dec_traffic_note = args.traffic, "given on the command line"
+        if dec_traffic is None:
+            dec_traffic = dram_traffic("decode_split_kernel_27b", held)
+            dec_traffic_note = ("ncu capture of this workload's split launch (bench.py --case "
+                                "decode_27b, one pass, cold L2)")
+        if dec_traffic is None:
+            dec_traffic = dram_traffic("decode_split_kernel", held)
+            dec_traffic_note = ("not measured on this launch: the DRAM bytes of the 8K-key "
+                                "capture (bench.py --case decode_8k), scaled by keys held")
         line = {
             "metric": METRIC,
             "value": round(value, 2),
@@ -841,8 +853,8 @@ def ours(args):
                 "peak_source": f"{peak_src} hbm_gbs",
                 "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4),
-                "traffic": args.traffic if args.traffic is not None else
-                dram_traffic("decode_split_kernel", int(x.kv_lens.sum()) * x.k_cache.shape[1]),
+                "traffic": dec_traffic,
+                "traffic_note": dec_traffic_note,
                 "avg_launch_ms": round(split_avg, 5),
                 "launch": split_launch,
                 "timing": "events around gqa_attn_decode_split alone in the step's form "
@@ -954,6 +966,9 @@ CASES = {
     # the 27B-shape prefill at full size (8192 causal rows, 24/4 heads, 320 MiB of
     # Q/K/V/G/out, ~0.53 ms per launch): for single-pass DRAM counters only
     "prefill_27b": lambda: S.WORKLOADS["prefill_27b"](),
+    # the 27B-shape decode at full size (16 sequences, kv lengths 1024..32768 in a
+    # [16,4,32768,256] cache, 2.1 GB; ~0.18 ms per split launch): single-pass counters only
+    "decode_27b": lambda: S.WORKLOADS["decode_27b"](),
 }
 
 
