@@ -148,7 +148,7 @@ def _sampled_rows(Hq, Lq, n, seed):
     for h in range(Hq):
         rows.add((0, h, Lq - 1))
         rows.add((0, h, 0))
-    while len(rows) < n:
+    while len(rows) < min(n, Hq * Lq):
         rows.add((0, int(rng.integers(Hq)), int(rng.integers(Lq))))
     return sorted(rows)
 
