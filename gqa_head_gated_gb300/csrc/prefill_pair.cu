@@ -454,6 +454,8 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (!ok) break;
         const float tmax = fmaxf(mx, sm.red[buf][half ^ 1][row]);
         bool store_ok = true;
+        bool late = false;        // fp16: O is rescaled by alpha_late after P_j is stored
+        float alpha_late = 1.f;
         if (j == 0) {
           m_run = tmax;
         } else if (__any_sync(0xffffffffu, tmax > m_run + rescale_threshold<kF16>())) {
@@ -462,18 +464,23 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           const float alpha = need ? ex2(m_run - tmax) : 1.f;
           if (need) m_run = tmax;
           l_part *= alpha;
-          // O must hold PV_{j-1} before it is rescaled.
-          store_ok = warp_all(ptx::mbar_wait(&sm.pv_done, (J - 1) & 1, tmo, &sm.abort));
-          if (store_ok) {
-            ptx::tc_fence_after();
+          if constexpr (kF16) {
+            late = true;          // warp-uniform, as the branch is
+            alpha_late = alpha;   // O is rescaled once P_j is stored (below)
+          } else {
+            // O must hold PV_{j-1} before it is rescaled.
+            store_ok = warp_all(ptx::mbar_wait(&sm.pv_done, (J - 1) & 1, tmo, &sm.abort));
+            if (store_ok) {
+              ptx::tc_fence_after();
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-              uint32_t o[32];
-              const uint32_t ta = trow + kTmO + 128u * half + 32u * cc;
-              ptx::tmem_ld32_wait(ta, o);
+              for (int cc = 0; cc < 4; ++cc) {
+                uint32_t o[32];
+                const uint32_t ta = trow + kTmO + 128u * half + 32u * cc;
+                ptx::tmem_ld32_wait(ta, o);
 #pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              ptx::tmem_st32_wait(ta, o);
+                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                ptx::tmem_st32_wait(ta, o);
+              }
             }
           }
         }
@@ -498,6 +505,17 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         l_part += (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
         const uint32_t pdst = trow + kTmS + uint32_t(kN) * buf + uint32_t(kHalf) * half;
         ptx::tmem_st32_wait(pdst, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        if constexpr (kF16) {
+          // fp16: O is rescaled after P_j is stored (see the one-CTA kernel)
+          if (late) {
+            if (!warp_all(ptx::mbar_wait(&sm.pv_done, (J - 1) & 1, tmo, &sm.abort))) {
+              fail(sm, p);
+              continue;  // the next exchange stops both threads of the pair
+            }
+            ptx::tc_fence_after();
+            rescale_o_cols(trow + kTmO + 128u * half, alpha_late);
+          }
+        }
         if constexpr (kClean) {
           // once V_j is cleaned: record, for its hit keys among this thread's keys,
           // whether the probability the product takes is 0 (read back from P)

@@ -40,6 +40,22 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
+// O *= alpha over this thread's 128 columns of O from tensor-memory address ta0 (the
+// fp16 kernels' lazy rescale, taken after P_j is stored).  Kept out of line so that
+// the softmax loop's registers are not shaped by it.  Warp-collective (called from a
+// warp-uniform branch).
+__device__ __noinline__ void rescale_o_cols(uint32_t ta0, float alpha) {
+#pragma unroll 1
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t o[32];
+    const uint32_t ta = ta0 + 32u * cc;
+    ptx::tmem_ld32_wait(ta, o);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+    ptx::tmem_st32_wait(ta, o);
+  }
+}
+
 // Position in a ring of tile slots [base, base + n): slot, phase bit, tiles so far.
 struct Ring {
   int slot;
