@@ -9,7 +9,9 @@
   Both in bf16 and in fp16 (the fp16 results also meet the fp16 bar).
   * A 3000-row prompt run in chunks whose last rows see 1024, 2047, 2048 and 3000
     keys (single CTAs for the first two, pairs for the rest) equals the whole-prompt
-    run: the prompt-row frames of the pages' prefill are cut at such seams."""
+    run bit for bit, in bf16 and fp16, with key outliers that make rows rescale; so
+    do a prompt cut into 16-row and into 32-row chunks, whose seams are those of the
+    pages' prompt-row frames."""
 import numpy as np
 import pytest
 import torch
@@ -17,7 +19,7 @@ import torch
 import gqa_head_gated_gb300 as G
 import oracle
 from synth import inputs as S
-from tests.parity import assert_parity, assert_parity_dtype, errors, to_f64
+from tests.parity import assert_parity_dtype, errors, to_f64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -85,25 +87,46 @@ def test_long_prompt_key_tile_edge(dtype, Lq, Hq, Hkv):
     _check_sampled(x, out, lse, rows, f"Lq {Lq}, {Hq}/{Hkv} heads")
 
 
-def test_chunked_equals_whole_across_pair_threshold():
-    x = S.make_prefill(1, 16, 2, 3000, seed=31)
-    whole, _, kernel = _run(x)
-    assert kernel == PAIR, kernel
+def _chunked(x, cuts):
+    """The prompt in chunks [c0, c1) at kv_offset c0; K / V hold the whole prompt (a
+    chunk's rows see keys 0..c0 + i of them).  Returns the rows and the kernels."""
     q, k, v, g = (t.to(DEV) for t in (x.q, x.k, x.v, x.g))
     parts, kernels = [], []
-    for c0, c1 in [(0, 1024), (1024, 2047), (2047, 2048), (2048, 3000)]:
-        # K / V hold the whole prompt; a chunk's rows see keys 0..c0 + i of them
+    for c0, c1 in cuts:
         parts.append(G.prefill(q[:, :, c0:c1].contiguous(), k, v, g[:, :, c0:c1].contiguous(),
                                kv_offset=c0))
         kernels.append(G.launch_log(1)[0]["kernel"])
     torch.cuda.synchronize()
     assert G.last_device_status() == 0
-    assert kernels == [SINGLE, SINGLE, PAIR, PAIR], kernels
-    chunked = torch.cat(parts, dim=2)
-    e = errors(chunked, whole.float())
-    assert e["max_abs"] <= 4e-3, e
+    return torch.cat(parts, dim=2), kernels
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=IDS)
+def test_chunked_equals_whole_across_pair_threshold(dtype):
+    single, pair = _names(dtype)
+    x = S.make_prefill(1, 16, 2, 3000, seed=31, outlier_frac=0.01, dtype=dtype)
+    whole, _, kernel = _run(x)
+    assert kernel == pair, kernel
+    chunked, kernels = _chunked(x, [(0, 1024), (1024, 2047), (2047, 2048), (2048, 3000)])
+    assert kernels == [single, single, pair, pair], kernels
+    assert torch.equal(chunked, whole), errors(chunked, whole.float())
     rows = _rows(16, 3000, 48, 31, extra=(1023, 1024, 2046, 2047, 2048))
     r_out, _ = oracle.prefill(to_f64(x.q), to_f64(x.k), to_f64(x.v), to_f64(x.g), kv_offset=0,
                               rows=rows)
     got = torch.stack([chunked[b, h, i] for b, h, i in rows])
-    assert_parity(got, r_out, "chunked across the pair threshold")
+    assert_parity_dtype(got, r_out, "chunked across the pair threshold")
+
+
+@pytest.mark.parametrize("step", [16, 32])
+@pytest.mark.parametrize("dtype", DTYPES, ids=IDS)
+def test_prompt_row_frames_equal_whole(dtype, step):
+    """A 2300-row prompt cut into frames of 16 or 32 rows (the first ones on single
+    CTAs, the frames whose last row sees 2048 keys or more on CTA pairs) equals the
+    whole-prompt run bit for bit."""
+    single, pair = _names(dtype)
+    x = S.make_prefill(1, 24, 4, 2300, seed=33, outlier_frac=0.01, dtype=dtype)
+    whole, _, _ = _run(x)
+    cuts = [(c, min(c + step, 2300)) for c in range(0, 2300, step)]
+    chunked, kernels = _chunked(x, cuts)
+    assert set(kernels) == {single, pair}, set(kernels)
+    assert torch.equal(chunked, whole), errors(chunked, whole.float())

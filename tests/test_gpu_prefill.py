@@ -94,7 +94,10 @@ def test_masked_future_keys_bit_exact():
 
 
 def test_chunked_equals_whole():
-    """A prompt run in chunks with kv_offset equals the whole-prompt run."""
+    """A prompt run in chunks with kv_offset equals the whole-prompt run bit for bit: a
+    row's arithmetic depends on its own scores and on the key tiles from key 0, not on
+    which row tile or CTA computes it (other rows' lazy rescales multiply it by exactly
+    1, and the keys it does not see add exact zeros)."""
     x = S.make_prefill(1, 16, 2, 700, seed=9)
     whole = run(x)
     q, k, v, g = (t.to(DEV) for t in (x.q, x.k, x.v, x.g))
@@ -103,8 +106,7 @@ def test_chunked_equals_whole():
         parts.append(G.prefill(q[:, :, c0:c1].contiguous(), k[:, :, :c1].contiguous(),
                                v[:, :, :c1].contiguous(), g[:, :, c0:c1].contiguous(), kv_offset=c0))
     chunked = torch.cat(parts, dim=2)
-    e = errors(chunked, whole.float())
-    assert e["max_abs"] <= 4e-3, e
+    assert torch.equal(chunked, whole), errors(chunked, whole.float())
 
 
 def test_one_key_too_far_control():
