@@ -51,7 +51,8 @@ constexpr int kKRingP = 2;                       // K ring: slots of 64 keys x 2
 constexpr int kVRingP = 2;                       // V ring: slots of 128 keys x 128 dims
 constexpr int kKHalfChunk = 64 * 128;            // K half: 64 keys x 64 dims per column block
 // Cleaning pass: a pair's candidate keys (the diagonal of its 2R rows and the rest of
-// its last key tile) are fewer than 384.
+// its last key tile) are fewer than 384 in bf16; in fp16 every key is a candidate, and
+// hit keys past the first 384 are left as they are.
 constexpr int kMaxHitsP = 384;
 
 template <bool kF16>
@@ -135,8 +136,10 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int rt_last = min(2 * pt + 1, p.n_rtiles - 1);
   const int key_end = p.kv_offset + min((rt_last + 1) * p.R, p.Lq);   // keys the pair's last row sees
   const int n_tiles = (key_end + kN - 1) / kN;
-  // first key some row of the pair does not see (the cleaning pass's candidates)
-  const int cand_lo = p.kv_offset + 2 * pt * p.R + 1;
+  // first key some row of the pair does not see (the cleaning pass's candidates); in
+  // fp16 every key (an fp16 P rounds to 0 more than 24 log2 units below the row
+  // maximum, where float64's p is not 0)
+  const int cand_lo = kF16 ? 0 : p.kv_offset + 2 * pt * p.R + 1;
   const uint32_t q_bytes = 4u * 128u * uint32_t(p.R * p.gqa);
 
   if (threadIdx.x == 0) {
@@ -493,8 +496,16 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         uint32_t pk[kHalf / 2];
         const float2 sc2 = make_float2(kScaleLog2, kScaleLog2);
         const float2 ms2 = make_float2(-msub, -msub);
+        // fp16 cleaning pass: bit c of zk = key c's score is -inf, i.e. its probability
+        // is exactly 0 (an fp16 P that rounds to 0 is not: see record_zero_scores)
+        uint32_t zk[2] = {0u, 0u};
 #pragma unroll
         for (int c = 0; c < kHalf / 2; ++c) {
+          if constexpr (kClean && kF16) {
+            zk[c >> 4] |= ((__uint_as_float(s[2 * c]) == -INFINITY ? 1u : 0u) |
+                           (__uint_as_float(s[2 * c + 1]) == -INFINITY ? 2u : 0u))
+                          << (2 * (c & 15));
+          }
           const float2 x = fma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
                                 sc2, ms2);
           const float p0 = ex2(x.x);
@@ -518,14 +529,17 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         if constexpr (kClean) {
           // once V_j is cleaned: record, for its hit keys among this thread's keys,
-          // whether the probability the product takes is 0 (read back from P)
+          // whether the probability is 0 (bf16: read back from P; fp16: a -inf score)
           if (warp_all(ptx::mbar_wait(&sm.vs_ready, uint32_t(j) & 1u, tmo, &sm.abort))) {
             const volatile uint32_t* th = sm.tile_hits[j & 1];
             const uint32_t w0 = th[2 * half], w1 = th[2 * half + 1];
-            if ((w0 | w1) != 0u)
-              record_zero_probs(sm, pdst, w0, w1,
-                                sm.tile_base[j & 1] + (half ? __popc(th[0]) + __popc(th[1]) : 0),
-                                row);
+            if ((w0 | w1) != 0u) {
+              const int idx = sm.tile_base[j & 1] + (half ? __popc(th[0]) + __popc(th[1]) : 0);
+              if constexpr (kF16)
+                record_zero_scores(sm, zk[0], zk[1], w0, w1, idx, row);
+              else
+                record_zero_probs(sm, pdst, w0, w1, idx, row);
+            }
           } else if (lane == 0) {
             fail(sm, p);   // the next exchange stops both threads of the pair
           }

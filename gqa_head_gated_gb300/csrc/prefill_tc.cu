@@ -82,8 +82,8 @@ constexpr int kThreads = 320;
 // Cleaning pass: keys whose V rows held a NaN / Inf element among the candidate keys
 // (see cand_lo in the kernel); at most kMaxHits per CTA are handled exactly (rows past
 // that are left as they are).  A causal prompt tile's candidates (its diagonal and the
-// rest of its last key tile) and a verify tile's are fewer than 256; a general mask
-// makes every key a candidate.
+// rest of its last key tile) and a verify tile's are fewer than 256; a general mask,
+// and fp16, make every key a candidate.
 constexpr int kMaxHits = 256;
 // General masks with one mask head for all query heads: the tile's mask rows (R query
 // rows x kN keys, each row padded by 16 bytes so that reads of different rows fall on
@@ -306,9 +306,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   // row; from it on (a causal prompt tile's diagonal, a verify tile's new keys past the
   // first row's, a tree's new keys, every key of a general mask, and every key of the
   // last tile past key_end) a V row can meet probability 0 in the P.V product.  The
-  // cleaning pass checks the V rows of these keys.
+  // cleaning pass checks the V rows of these keys.  In fp16 every key is a candidate:
+  // an fp16 P rounds to 0 more than 24 log2 units below the row maximum, where
+  // float64's p (and so p * Inf) is not 0.
   int cand_lo;
-  if constexpr (kMask)
+  if constexpr (kMask || kF16)
     cand_lo = 0;
   else if constexpr (!kSplit)
     cand_lo = p.kv_offset + r0 + 1;
@@ -842,8 +844,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         uint32_t pk[kHalf / 2];
         const float2 sc2 = make_float2(kScaleLog2, kScaleLog2);
         const float2 ms2 = make_float2(-msub, -msub);
+        // fp16 cleaning pass: bit c of zk = key c's score is -inf, i.e. its probability
+        // is exactly 0 (an fp16 P that rounds to 0 is not: see record_zero_scores)
+        uint32_t zk[2] = {0u, 0u};
 #pragma unroll
         for (int c = 0; c < kHalf / 2; ++c) {
+          if constexpr (kClean && kF16) {
+            zk[c >> 4] |= ((__uint_as_float(s[2 * c]) == -INFINITY ? 1u : 0u) |
+                           (__uint_as_float(s[2 * c + 1]) == -INFINITY ? 2u : 0u))
+                          << (2 * (c & 15));
+          }
           const float2 x = fma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
                                 sc2, ms2);
           const float p0 = ex2(x.x);
@@ -874,14 +884,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         if constexpr (kClean) {
           // Once V_j is cleaned: for its hit keys among this thread's keys, record
-          // whether the probability the P.V product takes is 0 (read back from P).
+          // whether the probability is 0 (bf16: read back from P; fp16: a -inf score).
           if (warp_all(ptx::mbar_wait(&sm.vs_ready[j & 1], (j >> 1) & 1, tmo, &sm.abort))) {
             const volatile uint32_t* th = sm.tile_hits[j & 1];
             const uint32_t w0 = th[2 * half], w1 = th[2 * half + 1];   // this half's keys
-            if ((w0 | w1) != 0u)
-              record_zero_probs(sm, pdst, w0, w1,
-                                sm.tile_base[j & 1] + (half ? __popc(th[0]) + __popc(th[1]) : 0),
-                                row);
+            if ((w0 | w1) != 0u) {
+              const int idx = sm.tile_base[j & 1] + (half ? __popc(th[0]) + __popc(th[1]) : 0);
+              if constexpr (kF16)
+                record_zero_scores(sm, zk[0], zk[1], w0, w1, idx, row);
+              else
+                record_zero_probs(sm, pdst, w0, w1, idx, row);
+            }
           } else if (lane == 0) {
             fail(sm, p);   // the next exchange stops both threads of the pair
           }

@@ -150,9 +150,12 @@ __device__ __noinline__ HitRows clean_rows(Sm& sm, uint8_t* vt, uint4 rows, int 
   return h;
 }
 
-// Reads this thread's 64 probabilities of a cleaned tile back from P in tensor memory
-// and records, for the hit keys among them (bits of w0, w1; hit-list indices from
-// idx), whether the probability the P.V product used was 0.  Whole warp.
+// Records, for the hit keys among this thread's 64 keys of a cleaned tile (bits of
+// w0, w1; hit-list indices from idx), whether the key's probability is 0, so that the
+// epilogue's p * V term is then a NaN and otherwise the value's own infinity.  bf16:
+// read back from P in tensor memory (a bf16 P is 0 exactly when the fp32 probability
+// is: the score is -inf, or more than 126 log2 units below the row maximum, where ex2
+// flushes to 0).  Whole warp.
 template <typename Sm>
 __device__ __noinline__ void record_zero_probs(Sm& sm, uint32_t p_taddr, uint32_t w0,
                                                uint32_t w1, int idx, int row) {
@@ -163,6 +166,22 @@ __device__ __noinline__ void record_zero_probs(Sm& sm, uint32_t p_taddr, uint32_
   for (int c = 0; c < kHalf; ++c) {
     if (((c < 32 ? w0 >> c : w1 >> (c - 32)) & 1u) != 0u) {
       if (((pw[c >> 1] >> ((c & 1) * 16)) & 0xFFFFu) == 0u)
+        atomicOr(&sm.pz[row][idx >> 5], 1u << (idx & 31));
+      ++idx;
+    }
+  }
+}
+
+// The same record for fp16, from the scores: an fp16 P rounds to 0 already 24 log2
+// units below the row maximum, where float64's p (and so p * Inf) is not 0, so a
+// probability counts as 0 only when the key's score is -inf (bits of z0, z1).
+template <typename Sm>
+__device__ __noinline__ void record_zero_scores(Sm& sm, uint32_t z0, uint32_t z1, uint32_t w0,
+                                                uint32_t w1, int idx, int row) {
+#pragma unroll 1
+  for (int c = 0; c < kHalf; ++c) {
+    if (((c < 32 ? w0 >> c : w1 >> (c - 32)) & 1u) != 0u) {
+      if (((c < 32 ? z0 >> c : z1 >> (c - 32)) & 1u) != 0u)
         atomicOr(&sm.pz[row][idx >> 5], 1u << (idx & 31));
       ++idx;
     }

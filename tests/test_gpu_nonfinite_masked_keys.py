@@ -101,6 +101,39 @@ def test_prefill_partially_masked_keys(case, dtype):
     assert_nonfinite_parity(lse, r_lse, f"prefill lse {case}", max_abs=2e-3, median_rel=1.0)
 
 
+# Key outliers (2 % of the keys x8) lift rows' maxima past the fp16 rescale threshold
+# (15 log2 units) again and again, so the cleaning pass rescales O while it cleans:
+# single CTAs (500 keys) and CTA pairs (2100 keys).
+RESCALING = {
+    "single_cta": ((1, 16, 2, 300, 500, 200),
+                   [("v_inf", 0, 205, 3), ("v_nan", 1, 330, 40), ("v_ninf", 1, 499, 255),
+                    ("k_nan", 0, 420, 9)]),
+    "cta_pair": ((1, 16, 2, 600, 2100, 1500),
+                 [("v_inf", 0, 1510, 3), ("v_nan", 1, 1800, 40), ("v_ninf", 1, 2099, 255),
+                  ("k_nan", 0, 1950, 9), ("v_nan", 0, 1501, 128)]),
+}
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "fp16"])
+@pytest.mark.parametrize("case", sorted(RESCALING))
+def test_prefill_rescaling_rows_partially_masked_keys(case, dtype):
+    (B, Hq, Hkv, Lq, Lkv, off), plants = RESCALING[case]
+    x = S.make_prefill(B, Hq, Hkv, Lq, Lkv=Lkv, kv_offset=off, seed=81, dtype=dtype,
+                       outlier_frac=0.02)
+    q, g = x.q.to(DEV), x.g.to(DEV)
+    clean = G.prefill(q, x.k.to(DEV), x.v.to(DEV), g, kv_offset=off)
+    kernel = G.launch_log(1)[0]["kernel"]
+    assert kernel.startswith("attn_pair_kernel" if case == "cta_pair" else "attn_tc_kernel"), kernel
+    _plant(x.k[0], x.v[0], plants)
+    out = G.prefill(q, x.k.to(DEV), x.v.to(DEV), g, kv_offset=off)
+    assert G.last_device_status() == 0
+    ref, _ = oracle.prefill(to_f64(x.q), to_f64(x.k), to_f64(x.v), to_f64(x.g), kv_offset=off)
+    gqa = Hq // Hkv
+    aff = _affected(lambda idx, gk, key: idx[1] // gqa == gk and key <= off + idx[2],
+                    plants, (B, Hq, Lq))
+    _check(out, clean, ref, aff, f"prefill with rescales {case}")
+
+
 # ----------------------------------------------------------------------------- verify
 VERIFY = {
     # 8 / 16 new rows x GQA 8: tcgen05 split kernel
