@@ -40,10 +40,11 @@
  *     of keys some of its rows do not see (in fp16 on the tensor-memory kernels:
  *     of every key, as an fp16 P rounds to 0 24 log2 units below the row's
  *     maximum) taken out of the tensor-core product and added back for the rows
- *     that see them.  Limits: the general-mask calls and the fp16 prefill handle
- *     up to 256 keys (384 on CTA pairs) with a non-finite V element per tile of
- *     query rows and KV head (every other call: any number); past that, rows that
- *     do not see the further keys may read NaN.  fp16 decode / verify groups of at
+ *     that see them.  Limits: the general-mask calls and the fp16 calls on the
+ *     tensor-memory kernels (prefill; decode / verify groups of 17 packed rows or
+ *     more) handle up to 256 keys (384 on CTA pairs) with a non-finite V element
+ *     per tile of query rows and KV head (every other call: any number); past
+ *     that, rows that do not see the further keys may read NaN.  fp16 decode / verify groups of at
  *     most 16 packed rows (the cp.async kernel): a visible +-Inf V value at a key
  *     more than 24 log2 units below the row's maximum gives NaN, not +-Inf.
  *   - Ownership: the caller owns every buffer.  The library never allocates
