@@ -44,9 +44,10 @@
  *     tensor-memory kernels (prefill; decode / verify groups of 17 packed rows or
  *     more) handle up to 256 keys (384 on CTA pairs) with a non-finite V element
  *     per tile of query rows and KV head (every other call: any number); past
- *     that, rows that do not see the further keys may read NaN.  fp16 decode / verify groups of at
- *     most 16 packed rows (the cp.async kernel): a visible +-Inf V value at a key
- *     more than 24 log2 units below the row's maximum gives NaN, not +-Inf.
+ *     that, rows that do not see the further keys may read NaN.  fp16 decode /
+ *     verify groups of at most 16 packed rows (the cp.async kernel): a visible
+ *     +-Inf V value at a key more than 24 log2 units below the row's maximum
+ *     gives NaN, not +-Inf.
  *   - Ownership: the caller owns every buffer.  The library never allocates
  *     device memory; the decode workspace is caller-provided.
  *   - Streams: every call is asynchronous on `stream` (may be 0 = legacy default
