@@ -137,7 +137,7 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int key_end = p.kv_offset + min((rt_last + 1) * p.R, p.Lq);   // keys the pair's last row sees
   const int n_tiles = (key_end + kN - 1) / kN;
   // first key some row of the pair does not see (the cleaning pass's candidates); in
-  // fp16 every key (an fp16 P rounds to 0 more than 24 log2 units below the row
+  // fp16 every key (an fp16 P rounds to 0 25 or more log2 units below the row
   // maximum, where float64's p is not 0)
   const int cand_lo = kF16 ? 0 : p.kv_offset + 2 * pt * p.R + 1;
   const uint32_t q_bytes = 4u * 128u * uint32_t(p.R * p.gqa);

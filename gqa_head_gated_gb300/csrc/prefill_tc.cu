@@ -307,7 +307,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   // first row's, a tree's new keys, every key of a general mask, and every key of the
   // last tile past key_end) a V row can meet probability 0 in the P.V product.  The
   // cleaning pass checks the V rows of these keys.  In fp16 every key is a candidate:
-  // an fp16 P rounds to 0 more than 24 log2 units below the row maximum, where
+  // an fp16 P rounds to 0 25 or more log2 units below the row maximum, where
   // float64's p (and so p * Inf) is not 0.
   int cand_lo;
   if constexpr (kMask || kF16)

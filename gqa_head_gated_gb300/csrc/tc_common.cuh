@@ -172,7 +172,7 @@ __device__ __noinline__ void record_zero_probs(Sm& sm, uint32_t p_taddr, uint32_
   }
 }
 
-// The same record for fp16, from the scores: an fp16 P rounds to 0 already 24 log2
+// The same record for fp16, from the scores: an fp16 P rounds to 0 already 25 log2
 // units below the row maximum, where float64's p (and so p * Inf) is not 0, so a
 // probability counts as 0 only when the key's score is -inf (bits of z0, z1).
 template <typename Sm>

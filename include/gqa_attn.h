@@ -38,7 +38,7 @@
  *     gives 0.  Finite inputs pay one check of each tile's outputs; a tile whose
  *     outputs hold a NaN / Inf is computed again with the non-finite V elements
  *     of keys some of its rows do not see (in fp16 on the tensor-memory kernels:
- *     of every key, as an fp16 P rounds to 0 24 log2 units below the row's
+ *     of every key, as an fp16 P rounds to 0 25 log2 units below the row's
  *     maximum) taken out of the tensor-core product and added back for the rows
  *     that see them.  Limits: the general-mask calls and the fp16 calls on the
  *     tensor-memory kernels (prefill; decode / verify groups of 17 packed rows or
@@ -46,7 +46,7 @@
  *     per tile of query rows and KV head (every other call: any number); past
  *     that, rows that do not see the further keys may read NaN.  fp16 decode /
  *     verify groups of at most 16 packed rows (the cp.async kernel): a visible
- *     +-Inf V value at a key more than 24 log2 units below the row's maximum
+ *     +-Inf V value at a key 25 or more log2 units below the row's maximum
  *     gives NaN, not +-Inf.
  *   - Ownership: the caller owns every buffer.  The library never allocates
  *     device memory; the decode workspace is caller-provided.
