@@ -169,3 +169,31 @@ def test_merge_nonfinite_parts(dtype):
     r_out, r_lse = oracle.lse_merge(o.double().numpy(), l.double().numpy())
     assert_nonfinite_parity(out, r_out, "merge")
     assert_nonfinite_parity(lse, r_lse, "merge lse", max_abs=1e-5, median_rel=1.0)
+
+
+@pytest.mark.parametrize("dtype,tc", [(torch.bfloat16, True), (torch.bfloat16, False),
+                                      (torch.float16, True)],
+                         ids=["bf16-tcgen05", "bf16-mma", "fp16-tcgen05"])
+def test_visible_inf_at_low_probability_key(dtype, tc):
+    """+Inf in V at a key every row sees whose probability is 2^-46 of the row
+    maximum's (key 60 = -u against key 50 = u, every query row of the group = u):
+    float64's p is tiny but positive, so that column is +Inf.  An fp16 P rounds such
+    a probability to 0; the tensor-memory kernel's fp16 cleaning pass still gives
+    +Inf.  (The cp.async kernel in fp16 gives NaN there, a stated limit; bf16 P keeps
+    probabilities down to 126 log2 units below the maximum.)"""
+    x = _decode_case(dtype, tc)
+    gqa = x.q.shape[1] // x.k_cache.shape[1]
+    r0, r1 = int(x.cu_rows[0]), int(x.cu_rows[1])
+    u = x.q[r0, gqa].clone()                              # sequence 0, KV head 1
+    x.q[r0:r1, gqa:2 * gqa] = u
+    x.k_cache[0, 1, 50] = u
+    x.k_cache[0, 1, 60] = -u
+    x.v_cache[0, 1, 60, 5] = INF
+    q, kc, vc, g, kv, cu = (t.to(DEV) for t in (x.q, x.k_cache, x.v_cache, x.g, x.kv_lens,
+                                                 x.cu_rows))
+    out = G.decode(q, kc, vc, g, kv, cu, max_rows=max(x.rows), max_kv_len=int(x.kv_lens.max()))
+    assert G.last_device_status() == 0
+    r_out, _ = oracle.decode(to_f64(x.q), to_f64(x.k_cache), to_f64(x.v_cache), to_f64(x.g),
+                             x.kv_lens.tolist(), x.cu_rows.tolist())
+    assert np.isposinf(r_out[r0:r1, gqa:2 * gqa, 5]).all()
+    assert_nonfinite_parity(out, r_out, "visible +Inf at a low-probability key")
