@@ -202,6 +202,35 @@ def test_chain_verify_partially_masked_keys(case, dtype):
 
 
 @pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "fp16"])
+def test_chain_verify_rescaling_rows_partially_masked_keys(dtype):
+    """The tcgen05 verify case with 2 % of the cached keys scaled x8 (rows rescale, and
+    keys far below a row's maximum round to an fp16 P of 0), the same plants plus a
+    +Inf value at an early key every row sees."""
+    (B, Hq, Hkv, rows, lens, Lcap), plants = VERIFY["tc"]
+    plants = plants + [(0, "v_inf", 1, 100, 7)]
+    x = S.make_decode(B, Hq, Hkv, rows, lens, Lcap=Lcap, seed=83, dtype=dtype)
+    gen = torch.Generator().manual_seed(83)
+    for b in range(B):
+        for gk in range(Hkv):
+            pos = torch.randperm(lens[b], generator=gen)[:max(1, lens[b] // 50)]
+            pos = pos[pos != 100]
+            x.k_cache[b, gk, pos] = (x.k_cache[b, gk, pos].float() * 8).to(dtype)
+    kw = dict(max_rows=max(rows), max_kv_len=max(lens))
+    clean = G.decode(*_decode_args(x), **kw)
+    assert any(r["kernel"].startswith("attn_tc_kernel<split") for r in G.launch_log(2))
+    _plant_decode(x, plants)
+    out = G.decode(*_decode_args(x), **kw)
+    assert G.last_device_status() == 0
+    ref, _ = oracle.decode(to_f64(x.q), to_f64(x.k_cache), to_f64(x.v_cache), to_f64(x.g),
+                           lens, x.cu_rows.tolist())
+    sees = _verify_sees(x)
+    aff = _affected(lambda idx, gk, bk: sees(idx, gk, bk),
+                    [(kind, gk, (b, key), col) for b, kind, gk, key, col in plants],
+                    tuple(x.q.shape[:2]))
+    _check(out, clean, ref, aff, "chain verify with rescales")
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "fp16"])
 @pytest.mark.parametrize("tc", [True, False], ids=["tcgen05", "mma"])
 def test_split_boundary_inside_new_keys(tc, dtype):
     """Fixed splits whose boundary falls among the new keys (split 1024 on the tcgen05
