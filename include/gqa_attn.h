@@ -48,7 +48,10 @@
  *     verify groups of at most 16 packed rows (the cp.async kernel): a visible
  *     +-Inf V value at a key 25 or more log2 units below the row's maximum
  *     gives NaN, not +-Inf.  Probabilities and merge weights are fp32: a key
- *     or split part more than 126 log2 units below the row's maximum weighs 0.
+ *     more than 126 log2 units below the row's maximum has probability 0 (a
+ *     +-Inf V value there gives NaN, except on the fp16 tensor-memory kernels),
+ *     and a split part that far below has merge weight 0 (its values do not
+ *     reach the output).
  *   - Ownership: the caller owns every buffer.  The library never allocates
  *     device memory; the decode workspace is caller-provided.
  *   - Streams: every call is asynchronous on `stream` (may be 0 = legacy default
